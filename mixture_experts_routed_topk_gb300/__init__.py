@@ -1,0 +1,28 @@
+"""Routed top-k mixture-of-experts expert layer (forward) for GB300 (sm_103a).
+
+The compute path is the C-ABI library ``libmoe_gb300.so`` (hand-written CUDA kernels); the
+functions re-exported here are its thin ctypes binding. Importing this package does not load the
+library: the first call does, and it raises if the library has not been built.
+"""
+
+__all__ = [
+    "moe_workspace_bytes",
+    "moe_workspace_layout",
+    "moe_routing",
+    "moe_fwd_dispatch",
+    "moe_fwd_gemm1",
+    "moe_fwd_gemm2",
+    "moe_fwd_combine",
+    "moe_routed_experts_fwd",
+    "moe_get_status",
+    "moe_status_string",
+    "MoeError",
+]
+
+
+def __getattr__(name):
+    if name in __all__:
+        from . import binding
+
+        return getattr(binding, name)
+    raise AttributeError(name)

@@ -1,0 +1,129 @@
+"""CPU oracle for the routed top-k expert layer -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference`` legs
+of ``bench.py`` may import this package. The product path (the CUDA library and its Python
+binding) never imports it, and shares no code with it.
+
+The arithmetic lives in ``moe_oracle.c`` (a plain per-token fp32 loop over bf16 inputs and a
+stable counting sort); this module compiles it with gcc and marshals numpy arrays to it. bf16
+tensors cross this boundary as their raw 16-bit patterns (``numpy.uint16``).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against brute force, closed forms
+and invariants, and ``tests/test_oracle_mutants.py`` checks that the pins catch planted mistakes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "moe_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+LIBRARY = os.path.join(_BUILD_DIR, "libmoe_oracle.so")
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", "-Wall"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_oracle(source: str, output: str) -> None:
+    """gcc the oracle source into a shared library (also used on patched copies by the tests)."""
+    os.makedirs(os.path.dirname(output), exist_ok=True)
+    tmp = output + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, source, "-lm"], check=True)
+    os.replace(tmp, output)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle if it is missing or older than its source. Returns the library path."""
+    if force or not os.path.exists(LIBRARY) or os.path.getmtime(LIBRARY) < os.path.getmtime(SOURCE):
+        compile_oracle(SOURCE, LIBRARY)
+    return LIBRARY
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    lib = ctypes.CDLL(path)
+    p = ctypes.c_void_p
+    lib.oracle_routing.argtypes = [p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, p, p, p, p]
+    lib.oracle_routing.restype = ctypes.c_long
+    lib.oracle_routed_experts.argtypes = [
+        p, p, p, ctypes.c_int, p, p, p,
+        ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int, ctypes.c_int,
+    ]
+    lib.oracle_routed_experts.restype = ctypes.c_int
+    return lib
+
+
+def _library(lib=None):
+    global _lib
+    if lib is not None:
+        return lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+        return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def routing(topk_ids: np.ndarray, num_experts: int, lib=None) -> dict:
+    """Expert counts, offsets and the stable permutation of the T*K (token, k) pairs.
+
+    Returns ``counts[E]``, ``offsets[E+1]``, ``perm[T*K]`` (row -> flat pair t*K+k),
+    ``inv[T*K]`` (flat pair -> row), all int32, and ``n_invalid`` (ids outside [0, E)).
+    """
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    if ids.ndim != 2:
+        raise ValueError("topk_ids must be [T, K]")
+    T, K = ids.shape
+    E = int(num_experts)
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    perm = np.zeros(T * K, np.int32)
+    inv = np.zeros(T * K, np.int32)
+    n_invalid = _library(lib).oracle_routing(
+        _ptr(ids), T, E, K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv)
+    )
+    if n_invalid < 0:
+        raise ValueError("oracle_routing rejected its arguments")
+    return {"counts": counts, "offsets": offsets, "perm": perm, "inv": inv, "n_invalid": int(n_invalid)}
+
+
+def routed_experts(x_bits, topk_ids, topk_scores, w13_bits, w2_bits, round_h: bool = False,
+                   nthreads: int | None = None, lib=None) -> np.ndarray:
+    """The layer's output ``out[T,D]`` in fp32.
+
+    ``x_bits`` [T,D], ``w13_bits`` [E,2,F,D] and ``w2_bits`` [E,D,F] are bf16 bit patterns
+    (uint16). ``topk_ids`` [T,K] int32. ``topk_scores`` [T,K] float32, or uint16 bf16 bits.
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    w13 = np.ascontiguousarray(w13_bits, dtype=np.uint16)
+    w2 = np.ascontiguousarray(w2_bits, dtype=np.uint16)
+    sc = np.asarray(topk_scores)
+    scores_bf16 = 1 if sc.dtype == np.uint16 else 0
+    sc = np.ascontiguousarray(sc, dtype=np.uint16 if scores_bf16 else np.float32)
+    T, D = x.shape
+    E, two, F, D2 = w13.shape
+    if two != 2 or D2 != D or w2.shape != (E, D, F) or ids.shape[0] != T or sc.shape != ids.shape:
+        raise ValueError("inconsistent shapes")
+    K = ids.shape[1]
+    out = np.zeros((T, D), np.float32)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _library(lib).oracle_routed_experts(
+        _ptr(x), _ptr(ids), _ptr(sc), scores_bf16, _ptr(w13), _ptr(w2), _ptr(out),
+        T, D, F, E, K, 1 if round_h else 0, int(nthreads),
+    )
+    if rc != 0:
+        raise RuntimeError("oracle_routed_experts failed")
+    return out

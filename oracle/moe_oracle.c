@@ -1,0 +1,241 @@
+/*
+ * moe_oracle.c -- CPU oracle for the routed top-k expert layer (forward pass).
+ *
+ * TEST INFRASTRUCTURE. Only tests/, __graft_entry__.smoke() and the CPU-baseline leg of bench.py
+ * load this library. The CUDA library never calls it, and the two share no code, header, table or
+ * helper: the only thing they have in common is the seeded input generator that feeds both.
+ *
+ * What it computes, for every token t (a plain per-token loop, no blocking or fusion):
+ *
+ *     out[t] = sum_{k<K} score[t,k] * W2[e] ( SiLU(Wg[e] x_t) * (Wu[e] x_t) ),   e = ids[t,k]
+ *
+ * Sources for the definition:
+ *   - Dist-MoE 0.1.0 (PyPI description), "Understand the execution model": the call routes rows,
+ *     then runs W13, SwiGLU, W2 and the combine; "BF16 Quickstart": the tensors x_TD,
+ *     topk_expert_ids_TK, topk_scores_TK, w13_E2FD ([E,2,F,D]), w2_EDF ([E,D,F]);
+ *     "Choose a precision and pipeline / BF16": BF16 operands, FP32 accumulation.
+ *   - TeraMoE README, worker list: the compute worker does the gate/up projection, the activation
+ *     and the down projection; the combine worker applies the final weighted accumulation.
+ *   - Primus MegaMoE technical guide, introduction and weight-module diagram: dispatch grouped GEMM
+ *     -> SwiGLU -> grouped GEMM with weighted reduce; w1 [g, 2I, H] holds gate then up, w2 [g, H, I].
+ *
+ * Precision: inputs are bf16 bit patterns, decoded here by a 16-bit shift; every product and sum
+ * is fp32, summed in ascending index order, as the pages' BF16 path accumulates in FP32. Built
+ * with -ffp-contract=off so no multiply-add is fused and x86 and Arm hosts give the same bits.
+ *
+ * Readings where the pages say nothing:
+ *   - w13[e,0] is the gate (goes through SiLU), w13[e,1] the up projection.
+ *   - SiLU(g) = g / (1 + exp(-g)) (the logistic-sigmoid-weighted linear unit), host libm expf.
+ *   - The score multiplies the expert output after W2, before the sum over k.
+ *   - An id outside [0, E) contributes nothing (the pages trap on bad input; this layer reports
+ *     it instead); duplicate ids within a token simply add.
+ *   - The routed order inside one expert's segment is ascending flat pair index t*K+k.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static float bf16_to_f32(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a float to the nearest bf16, ties to even (used only by the optional round_h mode, which
+ * mirrors a device path that stores the SwiGLU output in bf16). */
+static float round_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u) {
+        u &= 0xffff0000u; /* inf stays inf; a NaN keeps its top mantissa bits */
+        if ((u & 0x007f0000u) == 0 && (f != f)) u |= 0x00400000u;
+    } else {
+        u += 0x7fffu + ((u >> 16) & 1u);
+        u &= 0xffff0000u;
+    }
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * Routing (the local form of the pages' dispatch: "route on GPU" in Dist-MoE's execution model;
+ * "tokens are written directly to their expert-grouped positions" in the MoonEP FAQ).
+ *
+ * The R = T*K pairs i = t*K + k get the key key(i) = ids[i] if 0 <= ids[i] < E, else E.
+ *   counts[e]  = #{ i : key(i) = e }                          for e < E
+ *   offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]    (offsets[E] = number of valid pairs)
+ *   perm[r]    = the i of row r, rows sorted by (key(i), i) ascending (a stable counting sort;
+ *                invalid pairs fill rows offsets[E] .. R-1 in ascending i)
+ *   inv[i]     = the row of pair i, so inv[perm[r]] = r.
+ * Returns the number of invalid ids, or -1 on a bad argument.
+ */
+long oracle_routing(const int32_t *ids, int64_t T, int32_t E, int32_t K, int32_t *counts,
+                    int32_t *offsets, int32_t *perm, int32_t *inv) {
+    if (T < 0 || E <= 0 || K <= 0) return -1;
+    int64_t R = T * (int64_t)K;
+    int64_t *next = (int64_t *)calloc((size_t)E + 1, sizeof(int64_t));
+    int64_t *tally = (int64_t *)calloc((size_t)E + 1, sizeof(int64_t));
+    if (!next || !tally) {
+        free(next);
+        free(tally);
+        return -1;
+    }
+    long invalid = 0;
+    for (int64_t i = 0; i < R; ++i) {
+        int32_t e = ids[i];
+        if (e >= 0 && e < E) {
+            tally[e] += 1;
+        } else {
+            tally[E] += 1;
+            invalid += 1;
+        }
+    }
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e) {
+        counts[e] = (int32_t)tally[e];
+        offsets[e + 1] = offsets[e] + counts[e];
+    }
+    for (int32_t e = 0; e <= E; ++e) next[e] = (e < E) ? offsets[e] : offsets[E];
+    for (int64_t i = 0; i < R; ++i) {
+        int32_t e = ids[i];
+        int32_t key = (e >= 0 && e < E) ? e : E;
+        int64_t r = next[key]++;
+        perm[r] = (int32_t)i;
+        inv[i] = (int32_t)r;
+    }
+    free(next);
+    free(tally);
+    return invalid;
+}
+
+typedef struct {
+    const uint16_t *x;
+    const int32_t *ids;
+    const void *scores;
+    int scores_bf16;
+    const uint16_t *w13;
+    const uint16_t *w2;
+    float *out;
+    int64_t t_begin, t_end;
+    int32_t D, F, E, K;
+    int round_h;
+    int failed;
+} oracle_job;
+
+static float pair_score(const oracle_job *job, int64_t pair) {
+    if (job->scores_bf16) return bf16_to_f32(((const uint16_t *)job->scores)[pair]);
+    return ((const float *)job->scores)[pair];
+}
+
+/* The definition above, for tokens t_begin .. t_end-1. */
+static void *oracle_tokens(void *arg) {
+    oracle_job *job = (oracle_job *)arg;
+    const int32_t D = job->D, F = job->F, E = job->E, K = job->K;
+    float *xt = (float *)malloc(sizeof(float) * (size_t)D);
+    float *acc = (float *)malloc(sizeof(float) * (size_t)D);
+    float *h = (float *)malloc(sizeof(float) * (size_t)F);
+    if (!xt || !acc || !h) {
+        job->failed = 1;
+        free(xt);
+        free(acc);
+        free(h);
+        return NULL;
+    }
+    for (int64_t t = job->t_begin; t < job->t_end; ++t) {
+        for (int32_t d = 0; d < D; ++d) xt[d] = bf16_to_f32(job->x[t * D + d]);
+        for (int32_t j = 0; j < D; ++j) acc[j] = 0.0f;
+        for (int32_t k = 0; k < K; ++k) {
+            int32_t e = job->ids[t * K + k];
+            if (e < 0 || e >= E) continue;
+            float s = pair_score(job, t * K + k);
+            const uint16_t *wg = job->w13 + ((size_t)e * 2 + 0) * (size_t)F * (size_t)D;
+            const uint16_t *wu = job->w13 + ((size_t)e * 2 + 1) * (size_t)F * (size_t)D;
+            const uint16_t *w2e = job->w2 + (size_t)e * (size_t)D * (size_t)F;
+            /* gate/up projection and SwiGLU */
+            for (int32_t f = 0; f < F; ++f) {
+                float g = 0.0f, u = 0.0f;
+                for (int32_t d = 0; d < D; ++d) {
+                    g += bf16_to_f32(wg[(size_t)f * D + d]) * xt[d];
+                    u += bf16_to_f32(wu[(size_t)f * D + d]) * xt[d];
+                }
+                float silu = g / (1.0f + expf(-g));
+                h[f] = silu * u;
+                if (job->round_h) h[f] = round_to_bf16(h[f]);
+            }
+            /* down projection, weighted by the pair's score */
+            for (int32_t j = 0; j < D; ++j) {
+                float y = 0.0f;
+                for (int32_t f = 0; f < F; ++f) y += bf16_to_f32(w2e[(size_t)j * F + f]) * h[f];
+                acc[j] += s * y;
+            }
+        }
+        for (int32_t j = 0; j < D; ++j) job->out[t * D + j] = acc[j];
+    }
+    free(xt);
+    free(acc);
+    free(h);
+    return NULL;
+}
+
+/*
+ * out[T,D] (fp32) of the routed-experts forward. x [T,D], w13 [E,2,F,D] and w2 [E,D,F] are bf16
+ * bit patterns; ids [T,K] int32; scores [T,K] fp32 (scores_bf16 = 0) or bf16 bits (= 1).
+ * round_h = 1 rounds the SwiGLU output to bf16 before W2. Tokens are split across nthreads POSIX
+ * threads (each token is computed by one thread, in the same order, whatever nthreads is).
+ * Returns 0, or -1 on a bad argument or an allocation failure.
+ */
+int oracle_routed_experts(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
+                          const uint16_t *w13, const uint16_t *w2, float *out, int64_t T, int32_t D,
+                          int32_t F, int32_t E, int32_t K, int round_h, int nthreads) {
+    if (T < 0 || D <= 0 || F <= 0 || E <= 0 || K <= 0) return -1;
+    if (T == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > T) nthreads = (int)T;
+    oracle_job *jobs = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(jobs);
+        free(tids);
+        return -1;
+    }
+    int rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        oracle_job *j = &jobs[i];
+        j->x = x;
+        j->ids = ids;
+        j->scores = scores;
+        j->scores_bf16 = scores_bf16;
+        j->w13 = w13;
+        j->w2 = w2;
+        j->out = out;
+        j->t_begin = T * i / nthreads;
+        j->t_end = T * (i + 1) / nthreads;
+        j->D = D;
+        j->F = F;
+        j->E = E;
+        j->K = K;
+        j->round_h = round_h;
+    }
+    unsigned char *running = (unsigned char *)calloc((size_t)nthreads, 1);
+    if (!running) {
+        free(jobs);
+        free(tids);
+        return -1;
+    }
+    for (int i = 1; i < nthreads; ++i)
+        running[i] = (pthread_create(&tids[i], NULL, oracle_tokens, &jobs[i]) == 0);
+    oracle_tokens(&jobs[0]);
+    for (int i = 1; i < nthreads; ++i)
+        if (running[i]) pthread_join(tids[i], NULL);
+    for (int i = 1; i < nthreads; ++i)
+        if (!running[i]) oracle_tokens(&jobs[i]); /* could not start a thread: run its tokens here */
+    for (int i = 0; i < nthreads; ++i)
+        if (jobs[i].failed) rc = -1;
+    free(running);
+    free(jobs);
+    free(tids);
+    return rc;
+}

@@ -1,0 +1,56 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins catch each one.
+
+Every mutant is a textual patch of oracle/moe_oracle.c compiled into a temporary library; the
+real oracle is never modified. A mutant that no pin rejects would mean the pins are too weak.
+"""
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    "gate_up_swapped": [
+        ("wg = job->w13 + ((size_t)e * 2 + 0)", "wg = job->w13 + ((size_t)e * 2 + 1)"),
+        ("wu = job->w13 + ((size_t)e * 2 + 1)", "wu = job->w13 + ((size_t)e * 2 + 0)"),
+    ],
+    "score_dropped": [("acc[j] += s * y;", "acc[j] += y;")],
+    "silu_sign": [("expf(-g)", "expf(g)")],
+    "silu_wrong_slope": [("1.0f + expf(-g)", "1.0f + expf(-2.0f * g)")],
+    "w2_transposed": [("w2e[(size_t)j * F + f]", "w2e[(size_t)f * D + j]")],
+    "gate_transposed": [("wg[(size_t)f * D + d]", "wg[(size_t)d * F + f]")],
+    "last_k_dropped": [("for (int32_t k = 0; k < K; ++k)", "for (int32_t k = 0; k + 1 < K; ++k)")],
+    "wrong_token_row": [("job->x[t * D + d]", "job->x[((t + 1) % job->t_end) * D + d]")],
+    "up_not_multiplied": [("h[f] = silu * u;", "h[f] = silu;")],
+    "offsets_not_prefix": [("offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = counts[e];")],
+    "unstable_order": [
+        ("    for (int64_t i = 0; i < R; ++i) {\n        int32_t e = ids[i];\n        int32_t key",
+         "    for (int64_t i = R - 1; i >= 0; --i) {\n        int32_t e = ids[i];\n        int32_t key"),
+    ],
+    "invalid_ids_kept": [("int32_t key = (e >= 0 && e < E) ? e : E;", "int32_t key = (e >= 0 && e < E) ? e : 0;")],
+    "inv_identity": [("inv[i] = (int32_t)r;", "inv[i] = (int32_t)i;")],
+    "round_h_truncates": [("u += 0x7fffu + ((u >> 16) & 1u);", "u += 0u;")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    with open(oracle.SOURCE) as fh:
+        src = fh.read()
+    for old, new in MUTANTS[name]:
+        assert src.count(old) >= 1, f"patch anchor not found: {old!r}"
+        src = src.replace(old, new)
+    path = tmp_path / "mutant.c"
+    path.write_text(src)
+    lib_path = str(tmp_path / "libmutant.so")
+    oracle.compile_oracle(str(path), lib_path)
+    lib = oracle.load_library(lib_path)
+    failed = []
+    for check in oracle_pins.ALL_PINS:
+        try:
+            check(lib=lib)
+        except AssertionError:
+            failed.append(check.__name__)
+    assert failed, f"no pin rejects mutant {name}"

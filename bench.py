@@ -1,0 +1,513 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed top-k expert layer's forward pass on GB300.
+
+One step = one pass of the whole path over one batch: routing (histogram, scan, stable permute,
+row gather), the gate/up grouped GEMM with SwiGLU, the down grouped GEMM with the score
+weighting, and the combine -- through the C ABI, on inputs already resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0). Under torchrun each rank runs its own replica of the workload
+(tokens drawn with a rank-specific seed, the same weights): the path has no exchange step on one
+GPU per replica, so scaling is weak and no collective touches the data path; the ranks only meet
+at the barriers and the max-over-ranks reduction of the timings.
+
+--impl reference times the CPU oracle (test infrastructure, a deliberately plain C loop) on the
+box's host cores on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "routed-expert fwd tokens/s and TFLOP/s on 1 GB300; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+STAGES = ("dispatch", "gemm1_swiglu", "gemm2_score", "combine")
+KERNELS_PER_STEP = 7  # hist, scan, permute, gather, gemm1, gemm2, combine
+
+
+# ------------------------------------------------------------------------------ host logic
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=500)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--config", default="medium", choices=["tiny", "medium", "decode", "large", "skewed"])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host cores")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    """(rank, world, local_rank) from the torchrun environment (1 process when absent)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max(dist, value: float) -> float:
+    """Max of a float over ranks (identity for one process)."""
+    if dist is None:
+        return value
+    import torch
+
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Tokens and routing of each replica differ; weights use the base seed on every rank."""
+    return seed + 1009 * rank
+
+
+def measured_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            peaks = json.load(fh)
+        if peaks.get("hbm_gbs") and peaks.get("bf16_tflops"):
+            return peaks, "measured"
+    except (OSError, ValueError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_costs(T, D, F, E, K, touched):
+    """Algorithmic flops and bytes per launch of each stage (tile padding not counted)."""
+    R = T * K
+    return {
+        "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + 2 * R * D * 2},
+        "gemm1_swiglu": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * 2 + R * D * 2 + R * F * 2},
+        "gemm2_score": {"flops": 2 * R * D * F, "bytes": touched * D * F * 2 + R * F * 2 + R * D * 2 + R * 8},
+        "combine": {"flops": 0, "bytes": R * D * 2 + T * D * 2 + R * 4},
+    }
+
+
+def path_costs(T, D, F, E, K, touched):
+    """The layer's algorithmic flops and bytes: touched experts' weights, x, out, ids, scores."""
+    return 6 * T * K * D * F, touched * 3 * F * D * 2 + 2 * T * D * 2 + T * K * 8
+
+
+def roofline_entry(name, costs, seconds, peaks, sustained, traffic):
+    c = costs[name]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if c["flops"] > 0 and c["flops"] / max(c["bytes"], 1) >= ridge:
+        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        achieved = c["flops"] / seconds / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": name,
+                "peak_kind": "sustained" if sustained else "burst"}
+    achieved = c["bytes"] / seconds / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": name, "peak_kind": "copy"}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the grouped-GEMM sources; a recorded DRAM traffic is only valid for this hash."""
+    h = hashlib.sha256()
+    for rel in ("mixture_experts_routed_topk_gb300/csrc/grouped_gemm.cu",
+                "mixture_experts_routed_topk_gb300/csrc/ptx_sm103.cuh",
+                "mixture_experts_routed_topk_gb300/csrc/routing.cu",
+                "mixture_experts_routed_topk_gb300/csrc/combine.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str, kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture (profiles/dram_traffic.md), or None when
+    absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = kernel_source_hash()
+    for m in re.finditer(r"^\|\s*(\w+)\s*\|\s*(\w+)\s*\|\s*([0-9a-f]{16})\s*\|\s*([0-9.eE+]+)\s*\|", text, re.M):
+        if m.group(1) == config and m.group(2) == kernel and m.group(3) == src:
+            return float(m.group(4))
+    return None
+
+
+def assemble_line(**kw) -> str:
+    return json.dumps(kw, separators=(", ", ": "))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons, power = [], [], set(), []
+        for ln in self.lines:
+            f = [s.strip() for s in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [s for s, p in zip(sm, power) if p >= 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ------------------------------------------------------------------------------ oracle timing
+
+def oracle_sample(d, tokens: int):
+    """Host copies of the first `tokens` tokens and the experts they touch (ids renumbered)."""
+    import numpy as np
+    import torch
+
+    ids = d["topk_ids"][:tokens].cpu().numpy()
+    E = d["w13"].shape[0]
+    experts = np.unique(ids[(ids >= 0) & (ids < E)])
+    remap = np.full(E, -1, np.int64)
+    remap[experts] = np.arange(experts.size)
+    ex = torch.from_numpy(experts).to(d["w13"].device)
+    u16 = lambda t: t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    return {
+        "x": u16(d["x"][:tokens]),
+        "ids": remap[ids].astype(np.int32),
+        "scores": d["topk_scores"][:tokens].cpu().numpy().astype(np.float32),
+        "w13": u16(d["w13"].index_select(0, ex)),
+        "w2": u16(d["w2"].index_select(0, ex)),
+        "experts": int(experts.size),
+    }
+
+
+def oracle_tokens_for(seconds: float, wl, cores: int, gflops_per_core: float = 0.7) -> int:
+    per_token = 6.0 * wl.K * wl.D * wl.F
+    n = int(seconds * cores * gflops_per_core * 1e9 / per_token)
+    return max(1, min(n, wl.T))
+
+
+def bounded_tokens(ids_host, wl, n_tok: int, budget_bytes: int = 4 << 30) -> int:
+    """Shrink the token sample until the weights of the experts it touches fit the host budget."""
+    import numpy as np
+
+    per_expert = 3 * wl.F * wl.D * 2
+    while n_tok > 1:
+        first = ids_host[:n_tok]
+        touched = np.unique(first[(first >= 0) & (first < wl.E)]).size
+        if touched * per_expert <= budget_bytes:
+            break
+        n_tok = max(1, n_tok // 2)
+    return n_tok
+
+
+def time_oracle(sample, nthreads: int) -> float:
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.routed_experts(sample["x"], sample["ids"], sample["scores"], sample["w13"], sample["w2"],
+                          nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(d, wl, name: str, target_s: float) -> dict:
+    """The oracle as it stands on the host cores: a bounded token sample, repeated to fill about
+    target_s seconds; tokens/s = tokens processed / seconds."""
+    cores = os.cpu_count() or 1
+    ids_host = d["topk_ids"].cpu().numpy()
+    n_tok = bounded_tokens(ids_host, wl, oracle_tokens_for(target_s, wl, cores))
+    sample = oracle_sample(d, n_tok)
+    secs = [time_oracle(sample, cores)]
+    reps = max(1, min(100, int(target_s / max(secs[0], 1e-6))))
+    secs += [time_oracle(sample, cores) for _ in range(reps - 1)]
+    total = sum(secs)
+    return {"value": round(n_tok * len(secs) / total, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n_tok} tokens of the {name} workload ({sample['experts']} experts touched, full "
+                      f"K={wl.K} per token) x {len(secs)} runs = {total:.1f} s on {cores} threads",
+            "seconds": round(total, 2)}
+
+
+# ------------------------------------------------------------------------------ our path
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from mixture_experts_routed_topk_gb300 import binding, build
+    from mixture_experts_routed_topk_gb300 import workloads as W
+
+    build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+
+    wl = W.WORKLOADS[args.config]
+    T, D, F, E, K = wl.dims()
+    rseed = replica_seed(args.seed, rank)
+    x = W.make_x(T, D, rseed, device)
+    ids = W.make_topk_ids(T, E, K, wl.routing, rseed, device)
+    scores = W.make_scores(T, K, wl.scores, rseed, device)
+    w13, w2 = W.make_weights(E, D, F, args.seed, device)
+    dims = (T, D, F, E, K)
+    ws = binding.alloc_workspace(binding.moe_workspace_bytes(*dims), device)
+    out = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        binding.moe_fwd_dispatch(x, ids, dims, ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        binding.moe_fwd_gemm1(w13, dims, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        binding.moe_fwd_gemm2(scores, w2, dims, ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        binding.moe_fwd_combine(ids, out, dims, ws, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    status = binding.moe_get_status(ws, stream)
+    if status != 0:
+        raise RuntimeError(f"device status bits {status:#x} after warm-up")
+    counts = binding.moe_workspace_layout(*dims)
+    cnt = ws[counts["counts"]:counts["counts"] + 4 * E].view(torch.int32)
+    touched = int((cnt > 0).sum().item())
+
+    # ------------------------------------------------------------------ device-timed region
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid) if hasattr(
+        torch.cuda.get_device_properties(device), "uuid") else str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # outside the events: L2 holds no operand when a step starts
+        step(events[i])
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    barrier(dist, device)
+    sampler.stop()
+    stage_ms = {s: [events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps)]
+                for j, s in enumerate(STAGES)}
+    step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(args.steps)]
+    total_s = reduce_max(dist, sum(step_ms) / 1e3)
+
+    # ------------------------------------------------------------------ end to end (host buffers)
+    x_h = x.cpu().pin_memory()
+    ids_h = ids.cpu().pin_memory()
+    scores_h = scores.cpu().pin_memory()
+    out_h = torch.empty((T, D), dtype=torch.bfloat16).pin_memory()
+    x_d, ids_d, scores_d = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(scores)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        scores_d.copy_(scores_h, non_blocking=True)
+        binding.moe_routed_experts_fwd(x_d, ids_d, scores_d, w13, w2, out, ws, stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(args.warmup, 0)):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    e2e_s = reduce_max(dist, sum(e2e_ev[i][0].elapsed_time(e2e_ev[i][1]) for i in range(args.steps)) / 1e3)
+    h2d = x.numel() * 2 + ids.numel() * 4 + scores.numel() * 4
+    d2h = out.numel() * 2
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = measured_peaks()
+    costs = kernel_costs(T, D, F, E, K, touched)
+    mean_stage = {s: statistics.mean(v) for s, v in stage_ms.items()}
+    dominant = max(mean_stage, key=mean_stage.get)
+    ms_per_step = total_s * 1e3 / args.steps
+    sustained = ms_per_step * args.steps > 2000.0  # a seconds-long loop runs under the power cap
+    roof = roofline_entry(dominant, costs, mean_stage[dominant] / 1e3, peaks, sustained,
+                          recorded_traffic(args.config, dominant))
+    roof["peak_source"] = peak_src
+    flops, alg_bytes = path_costs(T, D, F, E, K, touched)
+    step_s = ms_per_step / 1e3
+    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline({"x": x, "topk_ids": ids, "topk_scores": scores, "w13": w13, "w2": w2}, wl,
+                           args.config, args.cpu_seconds)
+
+    line = assemble_line(
+        metric=METRIC,
+        value=round(world * T * args.steps / total_s, 1),
+        unit="tokens/s",
+        n_gpus=world,
+        steps=args.steps,
+        warmup=args.warmup,
+        ms_per_step=round(ms_per_step, 4),
+        higher_is_better=True,
+        scaling="weak",
+        vs_baseline=None,
+        dtype="bf16",
+        data="synthetic",
+        config={"workload": args.config, "T": T, "D": D, "F": F, "E": E, "K": K, "routing": wl.routing,
+                "experts_touched": touched, "global_batch": T * world, "parallelism": f"replicas{world}",
+                "l2": "flushed between steps (512 MB write)", "seed": args.seed},
+        tflops=round(world * flops / step_s / 1e12, 2),
+        path_roofline={"ms": round(t_roof * 1e3, 4), "frac": round(t_roof / step_s, 4),
+                       "flops": flops, "alg_bytes": alg_bytes},
+        roofline=roof,
+        stage_ms={s: round(v, 4) for s, v in mean_stage.items()},
+        e2e={"value": round(world * T * args.steps / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+             "d2h_bytes_per_step": d2h},
+        gpu_launches=KERNELS_PER_STEP * args.steps,
+        clocks=sampler.summary(),
+        wall_s=round(wall, 3),
+        cpu_baseline=cpu,
+    )
+    print(line, flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, world, local_rank):
+    """The CPU oracle as it stands, on the host cores, on bounded samples of the workload."""
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from mixture_experts_routed_topk_gb300 import workloads as W
+
+    oracle.build()
+    wl = W.WORKLOADS[args.config]
+    T, D, F, E, K = wl.dims()
+    cores = os.cpu_count() or 1
+    per_step_s = max(0.2, 60.0 / max(args.steps + args.warmup, 1))
+    dev = torch.device("cuda", local_rank) if torch.cuda.is_available() else torch.device("cpu")
+    x = W.make_x(T, D, args.seed, dev)
+    ids = W.make_topk_ids(T, E, K, wl.routing, args.seed, dev)
+    scores = W.make_scores(T, K, wl.scores, args.seed, dev)
+    n_tok = bounded_tokens(ids.cpu().numpy(), wl, oracle_tokens_for(per_step_s, wl, cores))
+    first = ids[:n_tok].cpu()
+    experts = sorted(set(first[(first >= 0) & (first < E)].tolist()))
+    w13, w2 = W.make_weights(E, D, F, args.seed, dev, experts=experts)
+    sample = oracle_sample({"x": x, "topk_ids": ids, "topk_scores": scores, "w13": w13, "w2": w2}, n_tok)
+    del w13, w2
+    for _ in range(max(args.warmup, 0)):
+        time_oracle(sample, cores)
+    secs = [time_oracle(sample, cores) for _ in range(args.steps)]
+    total = sum(secs)
+    value = round(n_tok * args.steps / total, 3)
+    desc = (f"each step: first {n_tok} tokens of the {args.config} workload ({sample['experts']} experts "
+            f"touched), full K={K} per token, on {cores} threads")
+    print(assemble_line(
+        impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=round(total * 1e3 / args.steps, 3), higher_is_better=True,
+        scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
+        config={"workload": args.config, "T": T, "D": D, "F": F, "E": E, "K": K, "routing": wl.routing,
+                "sample_tokens": n_tok},
+        cpu_baseline={"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+        e2e={"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    ), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world, local_rank)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * moe_routed_experts.h -- C ABI of the routed top-k mixture-of-experts expert layer (forward pass)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (the expert path shared by the TeraMoE README, Dist-MoE 0.1.0 and the Primus MegaMoE
+ * guide; the MoonEP page describes its weight layout):
+ *
+ *     out[t] = sum_{k<K} score[t,k] * W2[e] ( SiLU(Wg[e] x_t) * (Wu[e] x_t) ),   e = ids[t,k]
+ *
+ *  - Dist-MoE 0.1.0, "Understand the execution model": route on the GPU -> W13 -> SwiGLU -> W2 ->
+ *    combine. On one GPU the cross-rank "publish rows" / "combine" become a local stable permute of
+ *    the (token, k) pairs into expert-contiguous rows and a local weighted unpermute-and-sum.
+ *  - Dist-MoE 0.1.0, "BF16 Quickstart": the tensors x_TD [T,D], topk_expert_ids_TK [T,K],
+ *    topk_scores_TK [T,K], w13_E2FD [E,2,F,D] (also [E,2F,D] or [E*2F,D], the same memory),
+ *    w2_EDF [E,D,F] (also [E*D,F]); contiguous bf16 inputs and weights, expert ids in [0, E),
+ *    bf16 or fp32 scores. "Choose a precision and pipeline / BF16": bf16 operands, fp32
+ *    accumulation.
+ *  - Primus MegaMoE guide, weight-module diagram: w1 [g, 2I, H] is gate then up; w2 [g, H, I].
+ *  - MoonEP page, FAQ on the weight layout: one contiguous tensor per projection, experts addressed
+ *    by row offset -- the grouped GEMMs here address expert e at row e*2F of w13 and e*D of w2.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are CUDA device (or managed) memory on the current device; the
+ *    caller owns them and keeps them alive until the stream work that uses them has completed.
+ *  - bf16 is IEEE bfloat16 (16-bit storage). All arrays are dense row-major (C order).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream). No entry
+ *    point allocates memory, synchronises or copies device data to the host, except
+ *    moe_get_status, which synchronises `stream`.
+ *  - Host-side checks run before anything is enqueued; a non-MOE_OK return means nothing was
+ *    enqueued. Device-side problems never trap: they set bits in a status word that
+ *    moe_get_status reads.
+ *  - One workspace serves one call in flight at a time (sequentially reusable, not reentrant, as
+ *    the Dist-MoE context is).
+ *  - Shape limits (MOE_ERR_UNSUPPORTED_SHAPE otherwise): D and F multiples of 64; 1 <= E <= 4096;
+ *    K >= 1; T*K < 2^31; T >= 0 (T = 0 returns MOE_OK and enqueues nothing).
+ *  - Alignment (MOE_ERR_MISALIGNED otherwise): every pointer 16-byte aligned; the workspace
+ *    256-byte aligned.
+ */
+#ifndef MOE_ROUTED_EXPERTS_H
+#define MOE_ROUTED_EXPERTS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,         /* null pointer, negative size, unknown enum value */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* outside the shape limits above */
+    MOE_ERR_MISALIGNED = 3,          /* a pointer breaks the alignment rule above */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the size the call needs */
+    MOE_ERR_CUDA = 5,                /* a CUDA runtime or driver call failed */
+    MOE_ERR_UNSUPPORTED_DEVICE = 6   /* the current device is not sm_103 */
+} moe_status_t;
+
+/* Bits of the device status word (read with moe_get_status). */
+enum {
+    MOE_DEV_BAD_EXPERT_ID = 1u, /* an id outside [0, E): that (token, k) pair contributes 0 */
+    MOE_DEV_TIMEOUT = 2u        /* a kernel's bounded wait expired; its results are invalid */
+};
+
+/* Dtype of topk_scores. */
+enum { MOE_SCORES_F32 = 0, MOE_SCORES_BF16 = 1 };
+
+/* Regions of the forward workspace, for moe_workspace_layout. */
+enum {
+    MOE_WS_STATUS = 0,       /* uint32 device status word (always at byte offset 0)            */
+    MOE_WS_COUNTS = 1,       /* int32 [E]    rows routed to each expert                       */
+    MOE_WS_OFFSETS = 2,      /* int32 [E+1]  first row of each expert; [E] = valid pairs      */
+    MOE_WS_TILES1 = 3,       /* int32 [E+1]  prefix of the gate/up GEMM's tiles per expert     */
+    MOE_WS_TILES2 = 4,       /* int32 [E+1]  prefix of the down GEMM's tiles per expert        */
+    MOE_WS_BLOCK_COUNTS = 5, /* int32 [(E+1)*B]  per-(expert, routing block) counts            */
+    MOE_WS_BLOCK_BASES = 6,  /* int32 [(E+1)*B]  per-(expert, routing block) first rows        */
+    MOE_WS_PERM = 7,         /* int32 [T*K]  row -> flat pair t*K+k                            */
+    MOE_WS_INV = 8,          /* int32 [T*K]  flat pair -> row                                  */
+    MOE_WS_XP = 9,           /* bf16 [T*K, D] rows of x in routed order; after the down GEMM
+                                the same bytes hold Y [T, K, D], the score-weighted expert
+                                outputs per pair                                              */
+    MOE_WS_H = 10,           /* bf16 [T*K, F] SwiGLU output per routed row                     */
+    MOE_WS_TOTAL = 11,       /* total bytes (== moe_workspace_bytes)                          */
+    MOE_WS_REGIONS = 12
+};
+
+/*
+ * Bytes of device workspace that moe_routed_experts_fwd and the moe_fwd_* stages need for these
+ * sizes (0 for T = 0). Pure arithmetic; never touches the GPU. Returns 0 for sizes outside the
+ * shape limits.
+ */
+size_t moe_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K);
+
+/*
+ * Byte offsets of the workspace regions (MOE_WS_* above) into region_offsets[MOE_WS_REGIONS]
+ * (host memory, caller-owned). Each region starts on a 256-byte boundary. Pure arithmetic.
+ */
+moe_status_t moe_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                  size_t *region_offsets);
+
+/*
+ * Bytes of device workspace that moe_routing needs (status word and per-block scratch).
+ */
+size_t moe_routing_workspace_bytes(int64_t T, int32_t E, int32_t K);
+
+/*
+ * Routing alone: expert histogram, exclusive scan and stable permutation of the R = T*K
+ * (token, k) pairs (the local form of Dist-MoE's "route on GPU"; the MoonEP FAQ's "tokens are
+ * written directly to their expert-grouped positions").
+ *
+ *   topk_ids  device int32 [T,K]
+ *   counts    device int32 [E]    counts[e] = #{ pairs with id e }
+ *   offsets   device int32 [E+1]  offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
+ *   perm      device int32 [T*K]  perm[r] = t*K+k of the pair in row r; rows are ordered by
+ *                                 (expert, t*K+k) ascending; pairs with an id outside [0, E) fill
+ *                                 rows offsets[E] .. T*K-1 in ascending t*K+k
+ *   inv       device int32 [T*K]  inv[t*K+k] = its row
+ *   workspace device, moe_routing_workspace_bytes(T, E, K) bytes
+ * All four outputs are bit-exact (they are integers with a unique answer). An id outside [0, E)
+ * sets MOE_DEV_BAD_EXPERT_ID.
+ */
+moe_status_t moe_routing(const int32_t *topk_ids, int64_t T, int32_t E, int32_t K, int32_t *counts,
+                         int32_t *offsets, int32_t *perm, int32_t *inv, void *workspace,
+                         size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * The whole forward pass (Dist-MoE 0.1.0, "Understand the execution model"; TeraMoE README,
+ * compute and combine workers): routing, gate/up grouped GEMM with SwiGLU, down grouped GEMM with
+ * the score weighting, and a deterministic combine. Equivalent to moe_fwd_dispatch,
+ * moe_fwd_gemm1, moe_fwd_gemm2 and moe_fwd_combine in that order.
+ *
+ *   x            device bf16 [T,D]
+ *   topk_ids     device int32 [T,K]
+ *   topk_scores  device [T,K], fp32 (scores_dtype = MOE_SCORES_F32) or bf16 (MOE_SCORES_BF16)
+ *   w13          device bf16 [E,2,F,D]; w13[e,0] is the gate (through SiLU), w13[e,1] the up
+ *   w2           device bf16 [E,D,F]
+ *   out          device bf16 [T,D]; may not alias any input or the workspace
+ *   workspace    device, moe_workspace_bytes(T, D, F, E, K) bytes
+ *
+ * Numerics: bf16 operands, fp32 accumulation; the SwiGLU output H and the score-weighted pair
+ * outputs Y are rounded to bf16 (nearest even) in the workspace; the combine adds each token's K
+ * pair outputs in fp32 in k order and rounds once. The result is deterministic: repeated calls
+ * on the same inputs give the same bits. A pair with score 0 contributes exactly 0.
+ */
+moe_status_t moe_routed_experts_fwd(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                    int32_t scores_dtype, const void *w13, const void *w2, void *out,
+                                    int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                    void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Stage 1 of the forward pass: clears the status word, routes the pairs into the workspace's
+ * counts/offsets/perm/inv and tile lists, and copies x[t] into row inv[t*K+k] of the workspace's
+ * XP region (the expert-contiguous input of the gate/up GEMM).
+ */
+moe_status_t moe_fwd_dispatch(const void *x, const int32_t *topk_ids, int64_t T, int32_t D, int32_t F,
+                              int32_t E, int32_t K, void *workspace, size_t workspace_bytes,
+                              moe_stream_t stream);
+
+/*
+ * Stage 2: for every expert e, H[rows of e, :] = SiLU(XP_e Wg[e]^T) * (XP_e Wu[e]^T) (TeraMoE
+ * README, compute worker: gate/up projection and activation), into the workspace's H region.
+ * Needs stage 1's workspace contents.
+ */
+moe_status_t moe_fwd_gemm1(const void *w13, int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                           void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Stage 3: for every routed row r of expert e with pair p = perm[r],
+ * Y[p, :] = score[p] * (H[r, :] W2[e]^T) (the down projection with the pair's routing weight
+ * applied before the sum over k), into the workspace's XP region, which now holds Y [T,K,D].
+ * Needs stage 2's workspace contents.
+ */
+moe_status_t moe_fwd_gemm2(const void *topk_scores, int32_t scores_dtype, const void *w2, int64_t T,
+                           int32_t D, int32_t F, int32_t E, int32_t K, void *workspace,
+                           size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Stage 4: out[t, :] = bf16( sum_{k<K} Y[t, k, :] ) summed in fp32 in ascending k, skipping pairs
+ * whose id is outside [0, E) (TeraMoE README, combine and gather workers: the final weighted
+ * accumulation of a token's expert results). Needs stage 3's workspace contents.
+ */
+moe_status_t moe_fwd_combine(const int32_t *topk_ids, void *out, int64_t T, int32_t D, int32_t F,
+                             int32_t E, int32_t K, void *workspace, size_t workspace_bytes,
+                             moe_stream_t stream);
+
+/*
+ * Reads the device status word at the start of `workspace` (a forward or a routing workspace)
+ * into *device_bits (host memory): 0, or an OR of MOE_DEV_* bits raised since the last
+ * moe_fwd_dispatch / moe_routed_experts_fwd / moe_routing on that workspace. Synchronises
+ * `stream` first; the only synchronising entry point.
+ */
+moe_status_t moe_get_status(const void *workspace, uint32_t *device_bits, moe_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTED_EXPERTS_H */

@@ -8,6 +8,7 @@ library: the first call does, and it raises if the library has not been built.
 __all__ = [
     "moe_workspace_bytes",
     "moe_workspace_layout",
+    "moe_routing_workspace_bytes",
     "moe_routing",
     "moe_fwd_dispatch",
     "moe_fwd_gemm1",
@@ -17,6 +18,7 @@ __all__ = [
     "moe_get_status",
     "moe_status_string",
     "MoeError",
+    "alloc_workspace",
 ]
 
 

@@ -1,0 +1,213 @@
+"""ctypes binding of ``libmoe_gb300.so`` (the C ABI in ``include/moe_routed_experts.h``).
+
+Argument marshalling only: every function takes torch tensors, checks that they are what the C
+entry point expects (device, dtype, contiguity, shape), passes their device pointers and sizes to
+the entry point of the same name, and raises :class:`MoeError` on a non-``MOE_OK`` status. All
+computation runs in the library's CUDA kernels; there is no fallback of any kind, and a missing
+library raises at the first call.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_SCORES_F32 = 0
+MOE_SCORES_BF16 = 1
+MOE_DEV_BAD_EXPERT_ID = 1
+MOE_DEV_TIMEOUT = 2
+
+WS_REGIONS = (
+    "status", "counts", "offsets", "tiles1", "tiles2", "block_counts", "block_bases",
+    "perm", "inv", "xp", "h", "total",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn}: {message} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _build.LIBRARY
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"CUDA library {p} is missing; build it with mixture_experts_routed_topk_gb300.build.build()"
+            )
+        lib = ctypes.CDLL(p)
+        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        sig = {
+            "moe_workspace_bytes": ([i64, i32, i32, i32, i32], sz),
+            "moe_workspace_layout": ([i64, i32, i32, i32, i32, vp], ctypes.c_int),
+            "moe_routing_workspace_bytes": ([i64, i32, i32], sz),
+            "moe_routing": ([vp, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+            "moe_routed_experts_fwd": (
+                [vp, vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_fwd_dispatch": ([vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_fwd_gemm1": ([vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_fwd_gemm2": ([vp, i32, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_fwd_combine": ([vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_get_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
+            "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+        return lib
+
+
+def moe_status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MOE_OK:
+        raise MoeError(fn, status, moe_status_string(status))
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, ndim=None, cuda=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(x, topk_ids, w13):
+    T, D = x.shape
+    E, two, F, D2 = w13.shape
+    if two != 2 or D2 != D:
+        raise ValueError(f"w13 must be [E,2,F,D] with D={D}, got {tuple(w13.shape)}")
+    if topk_ids.shape[0] != T:
+        raise ValueError("topk_ids must be [T,K]")
+    return T, D, F, E, topk_ids.shape[1]
+
+
+# ----------------------------------------------------------------------------------- sizes
+
+def moe_workspace_bytes(T: int, D: int, F: int, E: int, K: int) -> int:
+    return int(load().moe_workspace_bytes(T, D, F, E, K))
+
+
+def moe_workspace_layout(T: int, D: int, F: int, E: int, K: int) -> dict:
+    arr = (ctypes.c_size_t * len(WS_REGIONS))()
+    _check("moe_workspace_layout", load().moe_workspace_layout(T, D, F, E, K, ctypes.cast(arr, ctypes.c_void_p)))
+    return dict(zip(WS_REGIONS, (int(v) for v in arr)))
+
+
+def moe_routing_workspace_bytes(T: int, E: int, K: int) -> int:
+    return int(load().moe_routing_workspace_bytes(T, E, K))
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A device byte buffer for the workspace (torch's allocator aligns it to 256 bytes or more)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ------------------------------------------------------------------------------ entry points
+
+def moe_routing(topk_ids, num_experts: int, counts, offsets, perm, inv, workspace, stream=None) -> None:
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    for name, t in (("counts", counts), ("offsets", offsets), ("perm", perm), ("inv", inv)):
+        _need(t, name, torch.int32)
+    _need(workspace, "workspace", torch.uint8)
+    T, K = topk_ids.shape
+    _check("moe_routing", load().moe_routing(
+        _ptr(topk_ids), T, int(num_experts), K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+        _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_routed_experts_fwd(x, topk_ids, topk_scores, w13, w2, out, workspace, stream=None) -> None:
+    _need(x, "x", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
+    _need(w13, "w13", torch.bfloat16, 4)
+    _need(w2, "w2", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 2)
+    _need(workspace, "workspace", torch.uint8)
+    T, D, F, E, K = _dims(x, topk_ids, w13)
+    if tuple(w2.shape) != (E, D, F) or tuple(out.shape) != (T, D) or tuple(topk_scores.shape) != (T, K):
+        raise ValueError("inconsistent shapes among w2 [E,D,F], out [T,D], topk_scores [T,K]")
+    sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
+    _check("moe_routed_experts_fwd", load().moe_routed_experts_fwd(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(out),
+        T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_fwd_dispatch(x, topk_ids, dims, workspace, stream=None) -> None:
+    _need(x, "x", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    T, D, F, E, K = dims
+    _check("moe_fwd_dispatch", load().moe_fwd_dispatch(
+        _ptr(x), _ptr(topk_ids), T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_fwd_gemm1(w13, dims, workspace, stream=None) -> None:
+    _need(w13, "w13", torch.bfloat16, 4)
+    T, D, F, E, K = dims
+    _check("moe_fwd_gemm1", load().moe_fwd_gemm1(
+        _ptr(w13), T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_fwd_gemm2(topk_scores, w2, dims, workspace, stream=None) -> None:
+    _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
+    _need(w2, "w2", torch.bfloat16, 3)
+    T, D, F, E, K = dims
+    sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
+    _check("moe_fwd_gemm2", load().moe_fwd_gemm2(
+        _ptr(topk_scores), sd, _ptr(w2), T, D, F, E, K, _ptr(workspace), workspace.numel(),
+        _stream_handle(stream)))
+
+
+def moe_fwd_combine(topk_ids, out, dims, workspace, stream=None) -> None:
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(out, "out", torch.bfloat16, 2)
+    T, D, F, E, K = dims
+    _check("moe_fwd_combine", load().moe_fwd_combine(
+        _ptr(topk_ids), _ptr(out), T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_get_status(workspace, stream=None) -> int:
+    """The device status bits of a workspace (synchronises the stream)."""
+    _need(workspace, "workspace", torch.uint8)
+    bits = ctypes.c_uint32(0)
+    _check("moe_get_status", load().moe_get_status(_ptr(workspace), ctypes.byref(bits), _stream_handle(stream)))
+    return int(bits.value)

@@ -1,0 +1,342 @@
+// moe_api.cu -- the C ABI (include/moe_routed_experts.h): argument checks, the workspace layout
+// and the launch sequence of the routed-experts forward pass.
+//
+// Every check that needs no GPU runs first, so a bad call returns before touching CUDA. After
+// that, the entry points only enqueue work on the caller's stream: no allocation, no host
+// synchronisation, no device-to-host copy (moe_get_status is the one synchronising call).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape limits shared by every entry point (D/F ignored when with_activations is false).
+moe_status_t check_shape(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool with_activations) {
+    if (T < 0 || E <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+    if (with_activations && (D <= 0 || F <= 0)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int64_t R = T * static_cast<int64_t>(K);
+    if (T > 0 && R / K != T) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (R >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (with_activations) {
+        if (D % 64 != 0 || F % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+        // TMA row coordinates and tile indices are 32-bit
+        if (static_cast<int64_t>(E) * 2 * F >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (static_cast<int64_t>(E) * D >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+        const int64_t ntn = ceil_div(F, kBN1) > ceil_div(D, kBN2) ? ceil_div(F, kBN1) : ceil_div(D, kBN2);
+        if ((ceil_div(R, kBM) + E) * ntn >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+bool make_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool with_activations, Layout* L) {
+    if (check_shape(T, D, F, E, K, with_activations) != MOE_OK) return false;
+    const int64_t R = T * static_cast<int64_t>(K);
+    L->nblk = static_cast<int>(ceil_div(R, kRouteChunk));
+    if (L->nblk < 1) L->nblk = 1;
+    const size_t e1 = static_cast<size_t>(E) + 1;
+    size_t sizes[MOE_WS_TOTAL] = {};
+    sizes[MOE_WS_STATUS] = sizeof(uint32_t);
+    sizes[MOE_WS_TILES1] = sizeof(int32_t) * e1;
+    sizes[MOE_WS_TILES2] = sizeof(int32_t) * e1;
+    sizes[MOE_WS_BLOCK_COUNTS] = sizeof(int32_t) * e1 * L->nblk;
+    sizes[MOE_WS_BLOCK_BASES] = sizeof(int32_t) * e1 * L->nblk;
+    if (with_activations) {
+        sizes[MOE_WS_COUNTS] = sizeof(int32_t) * E;
+        sizes[MOE_WS_OFFSETS] = sizeof(int32_t) * e1;
+        sizes[MOE_WS_PERM] = sizeof(int32_t) * R;
+        sizes[MOE_WS_INV] = sizeof(int32_t) * R;
+        sizes[MOE_WS_XP] = 2 * static_cast<size_t>(R) * D;
+        sizes[MOE_WS_H] = 2 * static_cast<size_t>(R) * F;
+    }
+    size_t off = 0;
+    for (int r = 0; r < MOE_WS_TOTAL; ++r) {
+        L->off[r] = off;
+        off += align_up(sizes[r]);
+    }
+    L->off[MOE_WS_TOTAL] = off;
+    return true;
+}
+
+moe_status_t device_info(DeviceInfo* info) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cached_sm[kMaxDevices];      // 0 = not queried yet
+    static std::atomic<int> cached_ok[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    int sm = cached_sm[dev].load(std::memory_order_acquire);
+    if (sm == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sm <= 0)
+            return MOE_ERR_CUDA;
+        cached_ok[dev].store(major == 10 && minor == 3 ? 1 : 0, std::memory_order_relaxed);
+        cached_sm[dev].store(sm, std::memory_order_release);
+    }
+    info->sm_count = sm;
+    info->supported = cached_ok[dev].load(std::memory_order_relaxed) != 0;
+    return MOE_OK;
+}
+
+namespace {
+
+struct Call {
+    Layout L;
+    DeviceInfo dev;
+    uint8_t* ws;
+    int64_t R;
+};
+
+// The common checks of the forward-pass stages. Host-only checks first; the device query last.
+moe_status_t prepare(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, void* workspace, size_t workspace_bytes,
+                     Call* c) {
+    moe_status_t st = check_shape(T, D, F, E, K, true);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;
+    if (!make_layout(T, D, F, E, K, true, &c->L)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (workspace_bytes < c->L.off[MOE_WS_TOTAL]) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    c->ws = static_cast<uint8_t*>(workspace);
+    c->R = T * static_cast<int64_t>(K);
+    return MOE_OK;
+}
+
+moe_status_t check_device(Call* c) {
+    moe_status_t st = device_info(&c->dev);
+    if (st != MOE_OK) return st;
+    return c->dev.supported ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+}
+
+template <typename P>
+P* region(const Call& c, int r) {
+    return reinterpret_cast<P*>(c.ws + c.L.off[r]);
+}
+
+GemmProblem gemm_problem(const Call& c, int32_t D, int32_t F, int32_t E, int which) {
+    GemmProblem p{};
+    p.R = c.R;
+    p.D = D;
+    p.F = F;
+    p.E = E;
+    p.counts = region<int32_t>(c, MOE_WS_COUNTS);
+    p.offsets = region<int32_t>(c, MOE_WS_OFFSETS);
+    p.tiles = region<int32_t>(c, which == 1 ? MOE_WS_TILES1 : MOE_WS_TILES2);
+    p.status = region<uint32_t>(c, MOE_WS_STATUS);
+    p.sm_count = c.dev.sm_count;
+    return p;
+}
+
+moe_status_t do_dispatch(const Call& c, const void* x, const int32_t* ids, int32_t D, int32_t F, int32_t E, int32_t K,
+                         cudaStream_t stream) {
+    if (cudaMemsetAsync(region<uint32_t>(c, MOE_WS_STATUS), 0, sizeof(uint32_t), stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    RoutingBuffers b{};
+    b.ids = ids;
+    b.R = c.R;
+    b.E = E;
+    b.nblk = c.L.nblk;
+    b.block_counts = region<int32_t>(c, MOE_WS_BLOCK_COUNTS);
+    b.block_bases = region<int32_t>(c, MOE_WS_BLOCK_BASES);
+    b.counts = region<int32_t>(c, MOE_WS_COUNTS);
+    b.offsets = region<int32_t>(c, MOE_WS_OFFSETS);
+    b.perm = region<int32_t>(c, MOE_WS_PERM);
+    b.inv = region<int32_t>(c, MOE_WS_INV);
+    b.tiles1 = region<int32_t>(c, MOE_WS_TILES1);
+    b.tiles2 = region<int32_t>(c, MOE_WS_TILES2);
+    b.ntiles_n1 = static_cast<int32_t>(ceil_div(F, kBN1));
+    b.ntiles_n2 = static_cast<int32_t>(ceil_div(D, kBN2));
+    b.status = region<uint32_t>(c, MOE_WS_STATUS);
+    moe_status_t st = launch_routing(b, stream);
+    if (st != MOE_OK) return st;
+    return launch_gather(x, b.perm, b.offsets, E, K, c.R, D, region<void>(c, MOE_WS_XP), c.dev.sm_count, stream);
+}
+
+moe_status_t do_gemm1(const Call& c, const void* w13, int32_t D, int32_t F, int32_t E, cudaStream_t stream) {
+    return launch_gemm1_swiglu(gemm_problem(c, D, F, E, 1), region<void>(c, MOE_WS_XP), w13, region<void>(c, MOE_WS_H),
+                               stream);
+}
+
+moe_status_t do_gemm2(const Call& c, const void* scores, int32_t scores_dtype, const void* w2, int32_t D, int32_t F,
+                      int32_t E, cudaStream_t stream) {
+    return launch_gemm2_score(gemm_problem(c, D, F, E, 2), region<void>(c, MOE_WS_H), w2,
+                              region<int32_t>(c, MOE_WS_PERM), scores, scores_dtype, region<void>(c, MOE_WS_XP),
+                              stream);
+}
+
+moe_status_t do_combine(const Call& c, const int32_t* ids, void* out, int64_t T, int32_t D, int32_t E, int32_t K,
+                        cudaStream_t stream) {
+    return launch_combine(region<void>(c, MOE_WS_XP), ids, T, D, E, K, out, c.dev.sm_count, stream);
+}
+
+bool bad_scores_dtype(int32_t d) { return d != MOE_SCORES_F32 && d != MOE_SCORES_BF16; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K) {
+    Layout L;
+    if (T == 0 || !make_layout(T, D, F, E, K, true, &L)) return 0;
+    return L.off[MOE_WS_TOTAL];
+}
+
+moe_status_t moe_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, size_t* region_offsets) {
+    if (region_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, D, F, E, K, true);
+    if (st != MOE_OK) return st;
+    Layout L;
+    if (!make_layout(T, D, F, E, K, true, &L)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    std::memcpy(region_offsets, L.off, sizeof(L.off));
+    return MOE_OK;
+}
+
+size_t moe_routing_workspace_bytes(int64_t T, int32_t E, int32_t K) {
+    Layout L;
+    if (T == 0 || !make_layout(T, 0, 0, E, K, false, &L)) return 0;
+    return L.off[MOE_WS_TOTAL];
+}
+
+moe_status_t moe_routing(const int32_t* topk_ids, int64_t T, int32_t E, int32_t K, int32_t* counts, int32_t* offsets,
+                         int32_t* perm, int32_t* inv, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    moe_status_t st = check_shape(T, 0, 0, E, K, false);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (!topk_ids || !counts || !offsets || !perm || !inv || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(topk_ids, 4) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm, 4) || !aligned(inv, 4))
+        return MOE_ERR_MISALIGNED;
+    if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;
+    Layout L;
+    if (!make_layout(T, 0, 0, E, K, false, &L)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (workspace_bytes < L.off[MOE_WS_TOTAL]) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo dev;
+    st = device_info(&dev);
+    if (st != MOE_OK) return st;
+    if (!dev.supported) return MOE_ERR_UNSUPPORTED_DEVICE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws + L.off[MOE_WS_STATUS], 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    RoutingBuffers b{};
+    b.ids = topk_ids;
+    b.R = T * static_cast<int64_t>(K);
+    b.E = E;
+    b.nblk = L.nblk;
+    b.block_counts = reinterpret_cast<int32_t*>(ws + L.off[MOE_WS_BLOCK_COUNTS]);
+    b.block_bases = reinterpret_cast<int32_t*>(ws + L.off[MOE_WS_BLOCK_BASES]);
+    b.counts = counts;
+    b.offsets = offsets;
+    b.perm = perm;
+    b.inv = inv;
+    b.status = reinterpret_cast<uint32_t*>(ws + L.off[MOE_WS_STATUS]);
+    return launch_routing(b, s);
+}
+
+moe_status_t moe_fwd_dispatch(const void* x, const int32_t* topk_ids, int64_t T, int32_t D, int32_t F, int32_t E,
+                              int32_t K, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Call c{};
+    moe_status_t st = prepare(T, D, F, E, K, workspace, workspace_bytes, &c);
+    if (st != MOE_OK || T == 0) return st;
+    if (!x || !topk_ids) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(topk_ids, 4)) return MOE_ERR_MISALIGNED;
+    if ((st = check_device(&c)) != MOE_OK) return st;
+    return do_dispatch(c, x, topk_ids, D, F, E, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_fwd_gemm1(const void* w13, int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream) {
+    Call c{};
+    moe_status_t st = prepare(T, D, F, E, K, workspace, workspace_bytes, &c);
+    if (st != MOE_OK || T == 0) return st;
+    if (!w13) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w13, 16)) return MOE_ERR_MISALIGNED;
+    if ((st = check_device(&c)) != MOE_OK) return st;
+    return do_gemm1(c, w13, D, F, E, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_fwd_gemm2(const void* topk_scores, int32_t scores_dtype, const void* w2, int64_t T, int32_t D,
+                           int32_t F, int32_t E, int32_t K, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream) {
+    Call c{};
+    if (bad_scores_dtype(scores_dtype)) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = prepare(T, D, F, E, K, workspace, workspace_bytes, &c);
+    if (st != MOE_OK || T == 0) return st;
+    if (!topk_scores || !w2) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w2, 16) || !aligned(topk_scores, scores_dtype == MOE_SCORES_F32 ? 4 : 2)) return MOE_ERR_MISALIGNED;
+    if ((st = check_device(&c)) != MOE_OK) return st;
+    return do_gemm2(c, topk_scores, scores_dtype, w2, D, F, E, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_fwd_combine(const int32_t* topk_ids, void* out, int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Call c{};
+    moe_status_t st = prepare(T, D, F, E, K, workspace, workspace_bytes, &c);
+    if (st != MOE_OK || T == 0) return st;
+    if (!topk_ids || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(topk_ids, 4)) return MOE_ERR_MISALIGNED;
+    if ((st = check_device(&c)) != MOE_OK) return st;
+    return do_combine(c, topk_ids, out, T, D, E, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_routed_experts_fwd(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                    int32_t scores_dtype, const void* w13, const void* w2, void* out, int64_t T,
+                                    int32_t D, int32_t F, int32_t E, int32_t K, void* workspace,
+                                    size_t workspace_bytes, moe_stream_t stream) {
+    Call c{};
+    if (bad_scores_dtype(scores_dtype)) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = prepare(T, D, F, E, K, workspace, workspace_bytes, &c);
+    if (st != MOE_OK || T == 0) return st;
+    if (!x || !topk_ids || !topk_scores || !w13 || !w2 || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) ||
+        !aligned(topk_scores, scores_dtype == MOE_SCORES_F32 ? 4 : 2))
+        return MOE_ERR_MISALIGNED;
+    if ((st = check_device(&c)) != MOE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = do_dispatch(c, x, topk_ids, D, F, E, K, s)) != MOE_OK) return st;
+    if ((st = do_gemm1(c, w13, D, F, E, s)) != MOE_OK) return st;
+    if ((st = do_gemm2(c, topk_scores, scores_dtype, w2, D, F, E, s)) != MOE_OK) return st;
+    return do_combine(c, topk_ids, out, T, D, E, K, s);
+}
+
+moe_status_t moe_get_status(const void* workspace, uint32_t* device_bits, moe_stream_t stream) {
+    if (!workspace || !device_bits) return MOE_ERR_INVALID_ARG;
+    if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;
+    if (cudaMemcpyAsync(&bits, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    *device_bits = bits;
+    return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null pointer, negative size or unknown enum value";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE: sizes outside the supported limits";
+        case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED: a pointer breaks the alignment rule";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL: workspace below the required size";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA runtime or driver call failed";
+        case MOE_ERR_UNSUPPORTED_DEVICE: return "MOE_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
+    }
+    return "unknown moe_status_t";
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// moe_internal.cuh -- constants, workspace layout and kernel launchers shared by the translation
+// units of the GB300 routed-experts library. Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "moe_routed_experts.h"
+
+namespace moe {
+
+// Routing: each routing block owns a contiguous chunk of (token, k) pairs; each of its warps owns
+// a contiguous 256-pair slice of that chunk, so ranks inside a block follow the pair order.
+constexpr int kRouteWarps = 8;
+constexpr int kRoutePairsPerWarp = 256;
+constexpr int kRouteChunk = kRouteWarps * kRoutePairsPerWarp;  // pairs per routing block
+constexpr int kMaxExperts = 4096;
+
+// Grouped GEMM tiles. Both GEMMs use a 128-row x 256-column fp32 accumulator in TMEM and walk K
+// in 64-element (128-byte) steps. The gate/up GEMM's 256 columns are 128 gate columns and the
+// same 128 up columns of one f range, so SwiGLU is local to one accumulator tile.
+constexpr int kBM = 128;
+constexpr int kBN1 = 128;  // f values per gate/up tile
+constexpr int kBN2 = 256;  // output columns per down tile
+constexpr int kBK = 64;
+
+struct Layout {
+    size_t off[MOE_WS_REGIONS];
+    int nblk;  // routing blocks
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Host: workspace layout for the forward pass (with_activations = true) or for moe_routing alone
+// (counts/offsets/perm/inv/XP/H regions empty; those arrays are the caller's).
+bool make_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool with_activations, Layout* L);
+
+// Host: per-device facts, queried once per device.
+struct DeviceInfo {
+    int sm_count;
+    bool supported;  // compute capability 10.3
+};
+moe_status_t device_info(DeviceInfo* info);
+
+// Kernel launchers (host). They enqueue on `stream` and return MOE_ERR_CUDA if a launch fails.
+struct RoutingBuffers {
+    const int32_t* ids;
+    int64_t R;
+    int32_t E;
+    int nblk;
+    int32_t* block_counts;
+    int32_t* block_bases;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    int32_t* inv;
+    int32_t* tiles1;  // may be null (moe_routing)
+    int32_t* tiles2;  // may be null
+    int32_t ntiles_n1;
+    int32_t ntiles_n2;
+    uint32_t* status;
+};
+moe_status_t launch_routing(const RoutingBuffers& b, cudaStream_t stream);
+
+moe_status_t launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int32_t E, int32_t K,
+                           int64_t R, int32_t D, void* xp, int sm_count, cudaStream_t stream);
+
+struct GemmProblem {
+    int64_t R;
+    int32_t D, F, E;
+    const int32_t* counts;
+    const int32_t* offsets;
+    const int32_t* tiles;
+    uint32_t* status;
+    int sm_count;
+};
+moe_status_t launch_gemm1_swiglu(const GemmProblem& p, const void* xp, const void* w13, void* h,
+                                 cudaStream_t stream);
+moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void* w2, const int32_t* perm,
+                                const void* scores, int32_t scores_dtype, void* y, cudaStream_t stream);
+
+moe_status_t launch_combine(const void* y, const int32_t* ids, int64_t T, int32_t D, int32_t E, int32_t K,
+                            void* out, int sm_count, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,110 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every declared symbol, and rejects
+bad arguments on the host before touching CUDA. Workspace layout arithmetic."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_routed_topk_gb300 import binding, build
+
+HEADER = os.path.join(build.INCLUDE, "moe_routed_experts.h")
+
+OK, INVALID, SHAPE, MISALIGNED, WS_SMALL = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("moe_workspace_bytes", "moe_routed_experts_fwd", "moe_routing", "moe_get_status",
+                     "moe_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = binding.moe_status_string(code)
+        assert s.startswith("MOE_")
+    assert "unknown" in binding.moe_status_string(99)
+
+
+FAKE = 1 << 20  # a 256-byte-aligned non-null address; never dereferenced (host checks fail first)
+
+
+def fwd(lib, **kw):
+    a = dict(x=FAKE, ids=FAKE, scores=FAKE, sd=0, w13=FAKE, w2=FAKE, out=FAKE,
+             T=16, D=256, F=256, E=8, K=2, ws=FAKE, wsb=1 << 40)
+    a.update(kw)
+    v = ctypes.c_void_p
+    return lib.moe_routed_experts_fwd(v(a["x"]), v(a["ids"]), v(a["scores"]), a["sd"], v(a["w13"]), v(a["w2"]),
+                                      v(a["out"]), a["T"], a["D"], a["F"], a["E"], a["K"], v(a["ws"]), a["wsb"], None)
+
+
+def test_host_validation_needs_no_gpu(lib):
+    assert fwd(lib, T=0) == OK  # nothing to do
+    assert fwd(lib, T=-1) == INVALID
+    assert fwd(lib, E=0) == INVALID
+    assert fwd(lib, K=0) == INVALID
+    assert fwd(lib, D=0) == INVALID
+    assert fwd(lib, sd=7) == INVALID
+    assert fwd(lib, x=0) == INVALID
+    assert fwd(lib, out=0) == INVALID
+    assert fwd(lib, ws=0) == INVALID
+    assert fwd(lib, D=200) == SHAPE
+    assert fwd(lib, F=96) == SHAPE
+    assert fwd(lib, E=4097) == SHAPE
+    assert fwd(lib, T=1 << 29, K=8) == SHAPE
+    assert fwd(lib, x=FAKE + 8) == MISALIGNED
+    assert fwd(lib, w2=FAKE + 4) == MISALIGNED
+    assert fwd(lib, ids=FAKE + 2) == MISALIGNED
+    assert fwd(lib, ws=FAKE + 16) == MISALIGNED
+    need = binding.moe_workspace_bytes(16, 256, 256, 8, 2)
+    assert fwd(lib, wsb=need - 1) == WS_SMALL
+
+
+def test_routing_host_validation(lib):
+    v = ctypes.c_void_p
+    r = lambda **kw: lib.moe_routing(v(kw.get("ids", FAKE)), kw.get("T", 4), kw.get("E", 4), kw.get("K", 2),
+                                     v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(kw.get("ws", FAKE)),
+                                     kw.get("wsb", 1 << 30), None)
+    assert r(T=0) == OK
+    assert r(ids=0) == INVALID
+    assert r(E=0) == INVALID
+    assert r(ids=FAKE + 1) == MISALIGNED
+    assert r(wsb=16) == WS_SMALL
+
+
+@pytest.mark.parametrize("dims", [(16, 256, 256, 8, 2), (4096, 2048, 1408, 64, 6), (64, 7168, 2048, 256, 8),
+                                  (16384, 7168, 2048, 256, 8), (1, 64, 64, 1, 1), (3, 64, 128, 4096, 7)])
+def test_workspace_layout(lib, dims):
+    T, D, F, E, K = dims
+    lay = binding.moe_workspace_layout(*dims)
+    R = T * K
+    sizes = {"status": 4, "counts": 4 * E, "offsets": 4 * (E + 1), "tiles1": 4 * (E + 1), "tiles2": 4 * (E + 1),
+             "perm": 4 * R, "inv": 4 * R, "xp": 2 * R * D, "h": 2 * R * F}
+    names = list(binding.WS_REGIONS)
+    for i, name in enumerate(names[:-1]):
+        assert lay[name] % 256 == 0
+        nxt = lay[names[i + 1]]
+        if name in sizes:
+            assert nxt - lay[name] >= sizes[name], name
+    assert lay["status"] == 0
+    assert lay["total"] == binding.moe_workspace_bytes(*dims)
+    assert binding.moe_routing_workspace_bytes(T, E, K) < lay["total"]

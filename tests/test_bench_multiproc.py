@@ -1,0 +1,75 @@
+"""The benchmark's multi-rank host logic on CPU: two gloo ranks, barrier, max over ranks, seeds."""
+
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, outdir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+
+    r, w, lr = bench.dist_env()
+    dist = bench.dist_init(w, "gloo")
+    bench.barrier(dist)
+    got = bench.reduce_max(dist, float(10 + 5 * r))
+    seed = bench.replica_seed(7, r)
+    with open(os.path.join(outdir, f"rank{r}.json"), "w") as fh:
+        json.dump({"rank": r, "world": w, "local": lr, "max": got, "seed": seed}, fh)
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True,
+                       start_method="spawn")
+    res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
+    assert [r["rank"] for r in res] == [0, 1]
+    assert all(r["world"] == 2 for r in res)
+    assert all(r["max"] == 15.0 for r in res)  # the max over ranks reaches every rank
+    assert res[0]["seed"] != res[1]["seed"]  # each replica draws its own tokens
+
+
+def test_single_process_defaults(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (0, 1, 0)
+    assert bench.dist_init(1, "gloo") is None
+    assert bench.reduce_max(None, 3.5) == 3.5
+    args = bench.parse_args([])
+    assert args.gpus == 1 and args.config == "medium" and args.impl == "ours" and args.warmup >= 3
+
+
+def test_roofline_arithmetic():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    peaks = {"hbm_gbs": 6790.0, "bf16_tflops": 1926.5, "bf16_tflops_sustained": 1735.9}
+    costs = bench.kernel_costs(4096, 2048, 1408, 64, 6, 64)
+    # gemm1: 4 R D F flops; compute bound at this size
+    r = bench.roofline_entry("gemm1_swiglu", costs, 1e-4, peaks, False, None)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 4 * 4096 * 6 * 2048 * 1408 / 1e-4 / 1e12) < 0.1
+    assert abs(r["frac"] - r["achieved"] / 1926.5) < 1e-3
+    c = bench.roofline_entry("combine", costs, 1e-4, peaks, False, None)
+    assert c["bound"] == "hbm" and c["unit"] == "GB/s"
+    flops, nbytes = bench.path_costs(4096, 2048, 1408, 64, 6, 64)
+    assert flops == 6 * 4096 * 6 * 2048 * 1408
+    assert nbytes == 64 * 3 * 1408 * 2048 * 2 + 2 * 4096 * 2048 * 2 + 4096 * 6 * 8

@@ -186,6 +186,38 @@ moe_status_t moe_fwd_combine(const int32_t *topk_ids, void *out, int64_t T, int3
                              int32_t E, int32_t K, void *workspace, size_t workspace_bytes,
                              moe_stream_t stream);
 
+/* Capacity of the library-owned scratch of moe_routing_static_scratch, in int32 entries per
+ * array: it serves sizes with (E + 1) * ceil(T*K / 2048) <= this value. */
+#define MOE_STATIC_SCRATCH_MAX_ENTRIES 262144
+
+/*
+ * Routing (the same results as moe_routing, bit for bit) without any caller-provided workspace.
+ * The pages have no counterpart: this entry point exists for callers that cannot allocate device
+ * memory at the point of the call -- for example an engine whose device memory is all owned and
+ * pre-planned by another allocator, or a plain C host program with no allocator at hand -- and so
+ * cannot pass moe_routing a workspace. It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ *   topk_ids, counts, offsets, perm, inv   as for moe_routing (device, caller-owned)
+ *   device_status  device uint32, caller-owned, or NULL: cleared, then receives the MOE_DEV_* bits
+ *                  of this call (an id outside [0, E) sets MOE_DEV_BAD_EXPERT_ID)
+ *
+ * Scratch: a fixed array inside the library (a file-scope __device__ variable of
+ * 2 * MOE_STATIC_SCRATCH_MAX_ENTRIES int32 plus 256 bytes, about 2 MiB), held on every GPU that
+ * loads the library until the process exits. Sizes with (E + 1) * ceil(T*K / 2048) above
+ * MOE_STATIC_SCRATCH_MAX_ENTRIES return MOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the array's device
+ * address with cudaGetSymbolAddress and caches it; make that first call before any stream
+ * capture. Every call on a device shares the one array and it keeps the previous call's
+ * contents; the call rewrites all of the scratch it reads. Calls whose GPU work overlaps (on
+ * different streams, or from different threads without ordering) race on the array: order them
+ * on one stream.
+ */
+moe_status_t moe_routing_static_scratch(const int32_t *topk_ids, int64_t T, int32_t E, int32_t K,
+                                        int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv,
+                                        uint32_t *device_status, moe_stream_t stream);
+
 /*
  * Reads the device status word at the start of `workspace` (a forward or a routing workspace)
  * into *device_bits (host memory): 0, or an OR of MOE_DEV_* bits raised since the last

@@ -67,6 +67,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "moe_fwd_gemm2": ([vp, i32, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
             "moe_fwd_combine": ([vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
             "moe_get_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
+            "moe_routing_static_scratch": ([vp, i64, i32, i32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -203,6 +204,26 @@ def moe_fwd_combine(topk_ids, out, dims, workspace, stream=None) -> None:
     T, D, F, E, K = dims
     _check("moe_fwd_combine", load().moe_fwd_combine(
         _ptr(topk_ids), _ptr(out), T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_routing_static_scratch(topk_ids, num_experts: int, counts, offsets, perm, inv, device_status=None,
+                               stream=None) -> None:
+    """Routing without a workspace: its scratch is a fixed ~2 MiB array inside the library.
+
+    For callers that cannot allocate device memory where they call the layer (an engine whose
+    device memory is all owned by another allocator, a host program with no allocator at hand).
+    The first call on a device looks up the array's address; make it before any stream capture.
+    Calls share the array, so calls whose GPU work overlaps race: order them on one stream.
+    """
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    for name, t in (("counts", counts), ("offsets", offsets), ("perm", perm), ("inv", inv)):
+        _need(t, name, torch.int32)
+    if device_status is not None:
+        _need(device_status, "device_status", (torch.int32, torch.uint8))
+    T, K = topk_ids.shape
+    _check("moe_routing_static_scratch", load().moe_routing_static_scratch(
+        _ptr(topk_ids), T, int(num_experts), K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+        _ptr(device_status), _stream_handle(stream)))
 
 
 def moe_get_status(workspace, stream=None) -> int:

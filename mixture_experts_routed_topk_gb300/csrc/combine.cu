@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "moe_internal.cuh"
+#include "ptx_sm103.cuh"
 
 namespace moe {
 namespace {
@@ -29,31 +30,30 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+template <typename Index>
 __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ y, const int32_t* __restrict__ ids,
-                                                 int64_t T, int32_t E, int32_t K, int vec_per_row,
+                                                 Index T, int32_t E, int32_t K, int32_t vec_per_row,
                                                  uint4* __restrict__ out) {
-    const int64_t total = T * vec_per_row;
-    const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += step) {
-        const int64_t t = v / vec_per_row;
-        const int64_t j = v - t * vec_per_row;
+    griddep_wait();
+    griddep_launch_dependents();
+    const Index total = T * vec_per_row;
+    const Index step = static_cast<Index>(gridDim.x) * blockDim.x;
+    for (Index v = static_cast<Index>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += step) {
+        const Index t = v / vec_per_row;
+        const Index j = v - t * vec_per_row;
+        const Index pair0 = t * K;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int k0 = 0; k0 < K; k0 += 8) {
-            uint4 q[8];
-            bool use[8];
+            int32_t e[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int k = k0 + u;
-                use[u] = false;
-                if (k < K) {
-                    const int32_t e = __ldg(ids + t * K + k);
-                    use[u] = (e >= 0 && e < E);
-                    if (use[u]) q[u] = __ldg(y + (t * K + k) * vec_per_row + j);
-                }
-            }
+            for (int u = 0; u < 8; ++u) e[u] = (k0 + u < K) ? __ldg(ids + pair0 + k0 + u) : -1;
+            uint4 q[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (use[u]) add_bf16x8(acc, q[u]);
+                if (e[u] >= 0 && e[u] < E) q[u] = __ldg(y + (pair0 + k0 + u) * vec_per_row + j);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (e[u] >= 0 && e[u] < E) add_bf16x8(acc, q[u]);
         }
         out[v] = make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]), pack2(acc[4], acc[5]),
                             pack2(acc[6], acc[7]));
@@ -69,9 +69,16 @@ moe_status_t launch_combine(const void* y, const int32_t* ids, int64_t T, int32_
     const int64_t want = ceil_div(total, 256);
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     const int grid = static_cast<int>(want < cap ? want : cap);
-    k_combine<<<grid > 0 ? grid : 1, 256, 0, stream>>>(static_cast<const uint4*>(y), ids, T, E, K, vec_per_row,
-                                                       static_cast<uint4*>(out));
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    const dim3 g(grid > 0 ? grid : 1), b(256);
+    const uint4* yv = static_cast<const uint4*>(y);
+    uint4* ov = static_cast<uint4*>(out);
+    cudaError_t err;
+    // 32-bit indexing when every index (and the grid-stride loop's overshoot) fits
+    if (T * K * static_cast<int64_t>(vec_per_row) + static_cast<int64_t>(grid) * 256 < (int64_t{1} << 31))
+        err = launch_pdl(k_combine<int32_t>, g, b, 0, stream, yv, ids, static_cast<int32_t>(T), E, K, vec_per_row, ov);
+    else
+        err = launch_pdl(k_combine<int64_t>, g, b, 0, stream, yv, ids, T, E, K, vec_per_row, ov);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

@@ -112,6 +112,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// The producer's walk over (tile, K step) pairs: tiles blockIdx.x, +gridDim.x, ...; K steps in order.
+struct StepCursor {
+    int32_t tile, kb;
+    Tile t;
+    int32_t brow0, brow1;
+};
+
+template <int kMode>
+__device__ __forceinline__ void cursor_enter_tile(StepCursor& c, const GemmArgs& a) {
+    c.t = decode_tile(c.tile, a);
+    if (kMode == 1) {
+        c.brow0 = c.t.e * 2 * a.F + c.t.n * kBN1;
+        c.brow1 = c.brow0 + a.F;
+    } else {
+        c.brow0 = c.t.e * a.D + c.t.n * kBN2;
+        c.brow1 = 0;
+    }
+}
+
+// Advances by one K step; returns false past the last tile.
+template <int kMode>
+__device__ __forceinline__ bool cursor_next(StepCursor& c, const GemmArgs& a, int32_t total) {
+    if (++c.kb < a.kblocks) return true;
+    c.kb = 0;
+    c.tile += gridDim.x;
+    if (c.tile >= total) return false;
+    cursor_enter_tile<kMode>(c, a);
+    return true;
+}
+
 template <int kMode>  // 1: gate/up + SwiGLU, 2: down + score
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -149,41 +179,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tcgen05_fence_before_sync();
     __syncthreads();
     tcgen05_fence_after_sync();
+    // everything above overlaps the previous kernel's tail; its outputs are read from here on
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = ps->tmem_base;
     const int32_t total = __ldg(args.tiles + args.E);
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && static_cast<int32_t>(blockIdx.x) < total) {
+            StepCursor ld{static_cast<int32_t>(blockIdx.x), 0, {}, 0, 0};
+            cursor_enter_tile<kMode>(ld, args);
             uint32_t it = 0;
-            bool ok = true;
-            for (int32_t tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, args);
-                int32_t brow0, brow1 = 0;
+            bool ok = true, more = true;
+            while (more) {
+                const uint32_t s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                if (!mbar_wait(&ps->empty[s], ph ^ 1u, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sa = smem + s * kStageBytes;
+                uint8_t* sb = sa + kABytes;
+                mbar_arrive_expect_tx(&ps->full[s], kStageBytes);
+                tma_load_2d(sa, &tmap_a, &ps->full[s], ld.kb * kBK, ld.t.row0);
                 if (kMode == 1) {
-                    brow0 = t.e * 2 * args.F + t.n * kBN1;
-                    brow1 = brow0 + args.F;
+                    tma_load_2d(sb, &tmap_b, &ps->full[s], ld.kb * kBK, ld.brow0);
+                    tma_load_2d(sb + kBBytes / 2, &tmap_b, &ps->full[s], ld.kb * kBK, ld.brow1);
                 } else {
-                    brow0 = t.e * args.D + t.n * kBN2;
+                    tma_load_2d(sb, &tmap_b, &ps->full[s], ld.kb * kBK, ld.brow0);
                 }
-                for (int32_t kb = 0; kb < args.kblocks; ++kb, ++it) {
-                    const uint32_t s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(&ps->empty[s], ph ^ 1u, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sa = smem + s * kStageBytes;
-                    uint8_t* sb = sa + kABytes;
-                    mbar_arrive_expect_tx(&ps->full[s], kStageBytes);
-                    tma_load_2d(sa, &tmap_a, &ps->full[s], kb * kBK, t.row0);
-                    if (kMode == 1) {
-                        tma_load_2d(sb, &tmap_b, &ps->full[s], kb * kBK, brow0);
-                        tma_load_2d(sb + kBBytes / 2, &tmap_b, &ps->full[s], kb * kBK, brow1);
-                    } else {
-                        tma_load_2d(sb, &tmap_b, &ps->full[s], kb * kBK, brow0);
-                    }
-                }
+                ++it;
+                more = cursor_next<kMode>(ld, args, total);
             }
             if (!ok) {
                 // aborting: give the copies already issued time to land before the CTA exits
@@ -398,8 +425,10 @@ moe_status_t launch_gemm1_swiglu(const GemmProblem& p, const void* xp, const voi
     a.H = static_cast<__nv_bfloat16*>(h);
     a.status = p.status;
     const int32_t ntn = static_cast<int32_t>(ceil_div(p.F, kBN1));
-    k_grouped_gemm<1><<<gemm_grid(p, ntn), kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, a);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_pdl(k_grouped_gemm<1>, dim3(gemm_grid(p, ntn)), dim3(kGemmThreads), kGemmSmemBytes, stream, ta, tb,
+                      a) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void* w2, const int32_t* perm,
@@ -424,8 +453,10 @@ moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void*
     a.Y = static_cast<__nv_bfloat16*>(y);
     a.status = p.status;
     const int32_t ntn = static_cast<int32_t>(ceil_div(p.D, kBN2));
-    k_grouped_gemm<2><<<gemm_grid(p, ntn), kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, a);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_pdl(k_grouped_gemm<2>, dim3(gemm_grid(p, ntn)), dim3(kGemmThreads), kGemmSmemBytes, stream, ta, tb,
+                      a) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

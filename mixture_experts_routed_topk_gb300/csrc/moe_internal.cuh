@@ -26,6 +26,26 @@ constexpr int kBN1 = 128;  // f values per gate/up tile
 constexpr int kBN2 = 256;  // output columns per down tile
 constexpr int kBK = 64;
 
+// Host: launches `kernel` with programmatic stream serialization, so its launch and prologue may
+// overlap the tail of the previous kernel on the stream. Every kernel launched this way calls
+// griddep_wait() before its first global memory access, so the stream order of memory effects is
+// unchanged.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct Layout {
     size_t off[MOE_WS_REGIONS];
     int nblk;  // routing blocks

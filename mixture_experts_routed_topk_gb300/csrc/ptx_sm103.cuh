@@ -25,6 +25,19 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
     return t;
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+
+// Blocks until the grids this one depends on (the previous kernel on the stream, when launched
+// with programmatic stream serialization) have completed and their memory is visible. Returns at
+// once when there is no such dependency. Every kernel calls it before its first global access.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel on the stream be scheduled once every CTA of this grid has issued it (or
+// exited); that kernel still waits in griddep_wait() for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

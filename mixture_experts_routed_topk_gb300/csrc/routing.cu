@@ -4,7 +4,7 @@
 //
 // Dist-MoE 0.1.0, "Understand the execution model": rows are routed on the GPU before W13. The
 // MoonEP FAQ on zero-copy: tokens are written straight to their expert-grouped positions, so the
-// gate/up GEMM reads them with no further copy.
+// gate/up GEMM reads them with plain tiled loads and no further copy.
 //
 // Every result here is an integer with a unique answer (the order inside an expert segment is
 // ascending pair index t*K+k), so the kernels are deterministic and bit-exact: counts come from
@@ -15,6 +15,7 @@
 #include <atomic>
 
 #include "moe_internal.cuh"
+#include "ptx_sm103.cuh"
 
 namespace moe {
 namespace {
@@ -27,6 +28,8 @@ __global__ void __launch_bounds__(256) k_route_hist(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ block_counts, uint32_t* status) {
     extern __shared__ int32_t hist[];  // [E+1]
     for (int i = threadIdx.x; i <= E; i += blockDim.x) hist[i] = 0;
+    griddep_wait();
+    griddep_launch_dependents();
     __syncthreads();
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
     const int64_t c1 = min(c0 + kRouteChunk, R);
@@ -79,6 +82,8 @@ __global__ void __launch_bounds__(1024) k_route_scan(const int32_t* __restrict__
                                                      int32_t* __restrict__ tiles2, int32_t ntn2) {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t total_mtiles;
+    griddep_wait();
+    griddep_launch_dependents();
     const int tid = threadIdx.x, nt = blockDim.x;
     const int64_t N = static_cast<int64_t>(E + 1) * nblk;
     const int64_t b0 = N * tid / nt, b1 = N * (tid + 1) / nt;
@@ -126,41 +131,50 @@ __global__ void __launch_bounds__(kRouteWarps * 32) k_route_permute(const int32_
                                                                     int32_t* __restrict__ perm,
                                                                     int32_t* __restrict__ inv) {
     extern __shared__ int32_t cnt[];  // [kRouteWarps][E+1]
+    constexpr int kRounds = kRoutePairsPerWarp / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stride = E + 1;
     for (int i = threadIdx.x; i < kRouteWarps * stride; i += blockDim.x) cnt[i] = 0;
-    __syncthreads();
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kRouteChunk + static_cast<int64_t>(warp) * kRoutePairsPerWarp;
+    // the warp's 256 keys, loaded once (all loads in flight together) and kept for both passes
+    int key[kRounds];
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        const int64_t i = base + r * 32 + lane;
+        key[r] = (i < R) ? route_key(__ldg(ids + i), E) : -1;
+    }
+    __syncthreads();
     int32_t* mine = cnt + warp * stride;
-    for (int r = 0; r < kRoutePairsPerWarp; r += 32) {
-        const int64_t i = base + r + lane;
-        const int key = (i < R) ? route_key(__ldg(ids + i), E) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        if (key >= 0 && lane == __ffs(peers) - 1) mine[key] += __popc(peers);
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        const unsigned peers = __match_any_sync(0xffffffffu, key[r]);
+        if (key[r] >= 0 && lane == __ffs(peers) - 1) mine[key[r]] += __popc(peers);
         __syncwarp();
     }
     __syncthreads();
-    for (int key = threadIdx.x; key <= E; key += blockDim.x) {
-        int32_t run = block_bases[static_cast<int64_t>(key) * nblk + blockIdx.x];
+    for (int k = threadIdx.x; k <= E; k += blockDim.x) {
+        int32_t run = block_bases[static_cast<int64_t>(k) * nblk + blockIdx.x];
         for (int w = 0; w < kRouteWarps; ++w) {
-            const int32_t c = cnt[w * stride + key];
-            cnt[w * stride + key] = run;
+            const int32_t c = cnt[w * stride + k];
+            cnt[w * stride + k] = run;
             run += c;
         }
     }
     __syncthreads();
     const unsigned lower = (1u << lane) - 1u;
-    for (int r = 0; r < kRoutePairsPerWarp; r += 32) {
-        const int64_t i = base + r + lane;
-        const int key = (i < R) ? route_key(__ldg(ids + i), E) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        if (key >= 0) {
-            const int32_t row = mine[key] + __popc(peers & lower);
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        const int64_t i = base + r * 32 + lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, key[r]);
+        if (key[r] >= 0) {
+            const int32_t row = mine[key[r]] + __popc(peers & lower);
             perm[row] = static_cast<int32_t>(i);
             inv[i] = row;
         }
         __syncwarp();
-        if (key >= 0 && lane == __ffs(peers) - 1) mine[key] += __popc(peers);
+        if (key[r] >= 0 && lane == __ffs(peers) - 1) mine[key[r]] += __popc(peers);
         __syncwarp();
     }
 }
@@ -170,6 +184,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) k_route_permute(const int32_
 __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                                                      const int32_t* __restrict__ offsets, int32_t E, int32_t K,
                                                      int vec_per_row, uint4* __restrict__ xp) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t nvalid = __ldg(offsets + E);
     const int lane = threadIdx.x & 31;
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -207,12 +223,14 @@ moe_status_t launch_routing(const RoutingBuffers& b, cudaStream_t stream) {
             return MOE_ERR_CUDA;
         g_permute_attr[dev].store(true, std::memory_order_release);
     }
-    k_route_hist<<<b.nblk, 256, hist_smem, stream>>>(b.ids, b.R, b.E, b.nblk, b.block_counts, b.status);
-    k_route_scan<<<1, 1024, 0, stream>>>(b.block_counts, b.block_bases, b.nblk, b.E, b.counts, b.offsets, b.tiles1,
-                                         b.ntiles_n1, b.tiles2, b.ntiles_n2);
-    k_route_permute<<<b.nblk, kRouteWarps * 32, perm_smem, stream>>>(b.ids, b.R, b.E, b.nblk, b.block_bases, b.perm,
-                                                                     b.inv);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (launch_pdl(k_route_hist, dim3(b.nblk), dim3(256), hist_smem, stream, b.ids, b.R, b.E, b.nblk, b.block_counts,
+                   b.status) != cudaSuccess ||
+        launch_pdl(k_route_scan, dim3(1), dim3(1024), 0, stream, b.block_counts, b.block_bases, b.nblk, b.E, b.counts,
+                   b.offsets, b.tiles1, b.ntiles_n1, b.tiles2, b.ntiles_n2) != cudaSuccess ||
+        launch_pdl(k_route_permute, dim3(b.nblk), dim3(kRouteWarps * 32), perm_smem, stream, b.ids, b.R, b.E, b.nblk,
+                   b.block_bases, b.perm, b.inv) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 moe_status_t launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int32_t E, int32_t K,
@@ -220,9 +238,10 @@ moe_status_t launch_gather(const void* x, const int32_t* perm, const int32_t* of
     const int vec_per_row = D / 8;
     const int64_t want = ceil_div(R, 8);  // one warp per row, 8 warps per block
     const int grid = static_cast<int>(want < static_cast<int64_t>(sm_count) * 8 ? want : static_cast<int64_t>(sm_count) * 8);
-    k_gather_rows<<<grid > 0 ? grid : 1, 256, 0, stream>>>(static_cast<const uint4*>(x), perm, offsets, E, K,
-                                                           vec_per_row, static_cast<uint4*>(xp));
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_pdl(k_gather_rows, dim3(grid > 0 ? grid : 1), dim3(256), 0, stream, static_cast<const uint4*>(x), perm,
+                      offsets, E, K, vec_per_row, static_cast<uint4*>(xp)) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

@@ -19,6 +19,7 @@ box's host cores on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -50,6 +51,8 @@ def parse_args(argv=None):
     p.add_argument("--config", default="medium", choices=["tiny", "medium", "decode", "large", "skewed"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--tokens", type=int, default=None,
+                   help="replace the workload's T (smaller cases for profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host cores")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     return p.parse_args(argv)
@@ -309,6 +312,8 @@ def run_ours(args, rank, world, local_rank):
     dist = dist_init(world, "nccl")
 
     wl = W.WORKLOADS[args.config]
+    if args.tokens:
+        wl = dataclasses.replace(wl, T=int(args.tokens))
     T, D, F, E, K = wl.dims()
     rseed = replica_seed(args.seed, rank)
     x = W.make_x(T, D, rseed, device)
@@ -371,8 +376,9 @@ def run_ours(args, rank, world, local_rank):
 
     # ------------------------------------------------------------------ end to end (host buffers)
     # Each step uploads its own x / ids / scores from pinned host memory and reads its output back,
-    # all inside the timed region. Uploads and read-backs run on a copy stream with two device
-    # input/output sets, so step i+1's upload overlaps step i's compute, as a serving loop would.
+    # all inside the timed region. Uploads and read-backs run on their own streams with two device
+    # input/output sets, so step i+1's upload and step i-1's read-back overlap step i's compute, as a
+    # serving loop would.
     x_h = [x.cpu().pin_memory() for _ in range(2)]
     ids_h = [ids.cpu().pin_memory() for _ in range(2)]
     scores_h = [scores.cpu().pin_memory() for _ in range(2)]
@@ -381,30 +387,37 @@ def run_ours(args, rank, world, local_rank):
     ids_d = [torch.empty_like(ids) for _ in range(2)]
     scores_d = [torch.empty_like(scores) for _ in range(2)]
     out_d = [torch.empty_like(out) for _ in range(2)]
-    copy_stream = torch.cuda.Stream(device)
+    up_stream = torch.cuda.Stream(device)    # host -> device uploads
+    down_stream = torch.cuda.Stream(device)  # device -> host read-backs
     uploaded = [torch.cuda.Event() for _ in range(2)]
     computed = [torch.cuda.Event() for _ in range(2)]
     read_back = [torch.cuda.Event() for _ in range(2)]
 
+    def upload(i):
+        b = i % 2
+        with torch.cuda.stream(up_stream):
+            if i >= 2:
+                up_stream.wait_event(computed[b])  # step i-2 has consumed this buffer set
+            x_d[b].copy_(x_h[b], non_blocking=True)
+            ids_d[b].copy_(ids_h[b], non_blocking=True)
+            scores_d[b].copy_(scores_h[b], non_blocking=True)
+            uploaded[b].record(up_stream)
+
     def e2e_run(n):
+        upload(0)
         for i in range(n):
             b = i % 2
-            with torch.cuda.stream(copy_stream):
-                if i >= 2:
-                    copy_stream.wait_event(computed[b])  # buffer b's previous step has been consumed
-                x_d[b].copy_(x_h[b], non_blocking=True)
-                ids_d[b].copy_(ids_h[b], non_blocking=True)
-                scores_d[b].copy_(scores_h[b], non_blocking=True)
-                uploaded[b].record(copy_stream)
             stream.wait_event(uploaded[b])
             if i >= 2:
                 stream.wait_event(read_back[b])  # out_d[b] of step i-2 has been read back
             binding.moe_routed_experts_fwd(x_d[b], ids_d[b], scores_d[b], w13, w2, out_d[b], ws, stream)
             computed[b].record(stream)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(computed[b])
+            if i + 1 < n:
+                upload(i + 1)  # overlaps this step's compute
+            with torch.cuda.stream(down_stream):
+                down_stream.wait_event(computed[b])
                 out_h[b].copy_(out_d[b], non_blocking=True)
-                read_back[b].record(copy_stream)
+                read_back[b].record(down_stream)
 
     e2e_run(max(args.warmup, 2))
     torch.cuda.synchronize(device)
@@ -413,9 +426,9 @@ def run_ours(args, rank, world, local_rank):
     barrier(dist, device)
     torch.cuda.synchronize(device)
     e2e_start.record(stream)
-    copy_stream.wait_event(e2e_start)
+    up_stream.wait_event(e2e_start)
     e2e_run(args.steps)
-    stream.wait_stream(copy_stream)
+    stream.wait_stream(down_stream)
     e2e_end.record(stream)
     torch.cuda.synchronize(device)
     barrier(dist, device)
@@ -459,8 +472,8 @@ def run_ours(args, rank, world, local_rank):
         vs_baseline=None,
         dtype="bf16",
         data="synthetic",
-        config={"workload": args.config, "T": T, "D": D, "F": F, "E": E, "K": K, "routing": wl.routing,
-                "experts_touched": touched, "global_batch": T * world, "parallelism": f"replicas{world}",
+        config={"workload": args.config if not args.tokens else f"{args.config} (T={T})", "T": T, "D": D, "F": F,
+                "E": E, "K": K, "routing": wl.routing, "experts_touched": touched, "global_batch": T * world, "parallelism": f"replicas{world}",
                 "l2": "flushed between steps (512 MB write)", "seed": args.seed},
         tflops=round(world * flops / step_s / 1e12, 2),
         path_roofline={"ms": round(t_roof * 1e3, 4), "frac": round(t_roof / step_s, 4),

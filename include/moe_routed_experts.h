@@ -226,6 +226,16 @@ moe_status_t moe_routing_static_scratch(const int32_t *topk_ids, int64_t T, int3
  */
 moe_status_t moe_get_status(const void *workspace, uint32_t *device_bits, moe_stream_t stream);
 
+/*
+ * Failure-detection self-test. Every wait inside the library's kernels is bounded; when one runs
+ * out the kernel sets MOE_DEV_TIMEOUT and returns instead of hanging. This launches one small
+ * kernel whose wait can never be satisfied (an mbarrier that nothing arrives on), bounded at
+ * timeout_us microseconds (1 .. 2000000), so that path can be checked on a GPU.
+ *   device_status  device uint32, caller-owned: cleared, then set to MOE_DEV_TIMEOUT
+ */
+moe_status_t moe_selftest_wait_timeout(uint32_t timeout_us, uint32_t *device_status,
+                                       moe_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *moe_status_string(moe_status_t status);
 

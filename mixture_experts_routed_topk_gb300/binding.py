@@ -68,6 +68,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "moe_fwd_combine": ([vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
             "moe_get_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
             "moe_routing_static_scratch": ([vp, i64, i32, i32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
+            "moe_selftest_wait_timeout": ([ctypes.c_uint32, vp, vp], ctypes.c_int),
             "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -224,6 +225,13 @@ def moe_routing_static_scratch(topk_ids, num_experts: int, counts, offsets, perm
     _check("moe_routing_static_scratch", load().moe_routing_static_scratch(
         _ptr(topk_ids), T, int(num_experts), K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
         _ptr(device_status), _stream_handle(stream)))
+
+
+def moe_selftest_wait_timeout(timeout_us: int, device_status, stream=None) -> None:
+    """Runs a kernel whose bounded wait must run out; device_status receives MOE_DEV_TIMEOUT."""
+    _need(device_status, "device_status", (torch.int32, torch.uint8))
+    _check("moe_selftest_wait_timeout", load().moe_selftest_wait_timeout(
+        int(timeout_us), _ptr(device_status), _stream_handle(stream)))
 
 
 def moe_get_status(workspace, stream=None) -> int:

@@ -73,7 +73,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete. Returns false (after setting the status
 // bit and the CTA abort flag) when the wait times out or another thread of the CTA has aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status, uint32_t timeout_bit) {
+                                          uint32_t* status, uint32_t timeout_bit,
+                                          unsigned long long timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
@@ -81,7 +82,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (global_timer_ns() - t0 > timeout_ns) {
             atomicOr(status, timeout_bit);
             *abort_flag = 1;
             return false;

@@ -58,6 +58,11 @@ def load_library(path: str) -> ctypes.CDLL:
         ctypes.c_int, ctypes.c_int,
     ]
     lib.oracle_routed_experts.restype = ctypes.c_int
+    lib.oracle_routed_experts_bwd.argtypes = [
+        p, p, p, ctypes.c_int, p, p, p, p, p, p, p,
+        ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+    ]
+    lib.oracle_routed_experts_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -126,4 +131,42 @@ def routed_experts(x_bits, topk_ids, topk_scores, w13_bits, w2_bits, round_h: bo
     )
     if rc != 0:
         raise RuntimeError("oracle_routed_experts failed")
+    return out
+
+
+def routed_experts_bwd(x_bits, topk_ids, topk_scores, w13_bits, w2_bits, dout, nthreads: int | None = None,
+                       lib=None) -> dict:
+    """Gradients of the layer for the upstream gradient ``dout`` [T,D] (float32).
+
+    Returns fp32 ``dx`` [T,D], ``dscores`` [T,K], ``dw13`` [E,2,F,D] and ``dw2`` [E,D,F].
+    Inputs as for :func:`routed_experts`.
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    w13 = np.ascontiguousarray(w13_bits, dtype=np.uint16)
+    w2 = np.ascontiguousarray(w2_bits, dtype=np.uint16)
+    go = np.ascontiguousarray(dout, dtype=np.float32)
+    sc = np.asarray(topk_scores)
+    scores_bf16 = 1 if sc.dtype == np.uint16 else 0
+    sc = np.ascontiguousarray(sc, dtype=np.uint16 if scores_bf16 else np.float32)
+    T, D = x.shape
+    E, two, F, _ = w13.shape
+    K = ids.shape[1]
+    if two != 2 or w2.shape != (E, D, F) or go.shape != (T, D) or sc.shape != ids.shape:
+        raise ValueError("inconsistent shapes")
+    out = {
+        "dx": np.zeros((T, D), np.float32),
+        "dscores": np.zeros((T, K), np.float32),
+        "dw13": np.zeros((E, 2, F, D), np.float32),
+        "dw2": np.zeros((E, D, F), np.float32),
+    }
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _library(lib).oracle_routed_experts_bwd(
+        _ptr(x), _ptr(ids), _ptr(sc), scores_bf16, _ptr(w13), _ptr(w2), _ptr(go),
+        _ptr(out["dx"]), _ptr(out["dscores"]), _ptr(out["dw13"]), _ptr(out["dw2"]),
+        T, D, F, E, K, int(nthreads),
+    )
+    if rc != 0:
+        raise RuntimeError("oracle_routed_experts_bwd failed")
     return out

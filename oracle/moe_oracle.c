@@ -23,6 +23,11 @@
  * is fp32, summed in ascending index order, as the pages' BF16 path accumulates in FP32. Built
  * with -ffp-contract=off so no multiply-add is fused and x86 and Arm hosts give the same bits.
  *
+ * The backward pass (oracle_routed_experts_bwd, at the end of this file) is the same definition
+ * differentiated by hand; the pages name its parts (Dist-MoE 0.1.0, "Understand the execution
+ * model": DGRAD computes input gradients and WGRAD weight gradients; TeraMoE README, usage
+ * example: output.backward(...)).
+ *
  * Readings where the pages say nothing:
  *   - w13[e,0] is the gate (goes through SiLU), w13[e,1] the up projection.
  *   - SiLU(g) = g / (1 + exp(-g)) (the logistic-sigmoid-weighted linear unit), host libm expf.
@@ -237,5 +242,220 @@ int oracle_routed_experts(const uint16_t *x, const int32_t *ids, const void *sco
     free(running);
     free(jobs);
     free(tids);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Backward pass.                                                                              */
+/*                                                                                             */
+/* For a pair p = (t, k) with e = ids[p], s = scores[p] and upstream gradient dout[t] (D):     */
+/*   g = Wg[e] x_t, u = Wu[e] x_t, a = SiLU(g), h = a * u, y = W2[e] h     (the forward)      */
+/*   dscores[p]  = <dout[t], y>                                                                */
+/*   dh          = s * W2[e]^T dout[t]                                                      */
+/*   dg          = dh * u * SiLU'(g),  SiLU'(g) = sig(g) (1 + g (1 - sig(g)))             */
+/*   du          = dh * a                                                                     */
+/*   dx[t]      += Wg[e]^T dg + Wu[e]^T du                                                    */
+/*   dW2[e]     += (s * dout[t]) h^T                                                           */
+/*   dWg[e]     += dg x_t^T,   dWu[e] += du x_t^T                                             */
+/* Pairs with ids outside [0, E) contribute nothing and get dscores = 0.                       */
+/* Pass A (tokens in parallel) gives dx and dscores; pass B (experts in parallel) gives the     */
+/* weight gradients, summing each expert's pairs in ascending t*K+k. All of it in fp32.        */
+
+typedef struct {
+    const oracle_job *fw; /* shapes and forward inputs */
+    const float *dout;
+    float *dx, *dscores, *dw13, *dw2;
+    int32_t e_begin, e_end; /* pass B range */
+    int failed;
+} oracle_bwd_job;
+
+/* g, u, a, h and W2^T dout[t] for one pair (the shared recomputation of both passes). */
+static void pair_recompute(const oracle_job *fw, const float *xt, const float *dout_t, int32_t e,
+                           float *g, float *u, float *a, float *h, float *w2t_dout) {
+    const int32_t D = fw->D, F = fw->F;
+    const uint16_t *wg = fw->w13 + ((size_t)e * 2 + 0) * (size_t)F * (size_t)D;
+    const uint16_t *wu = fw->w13 + ((size_t)e * 2 + 1) * (size_t)F * (size_t)D;
+    const uint16_t *w2e = fw->w2 + (size_t)e * (size_t)D * (size_t)F;
+    for (int32_t f = 0; f < F; ++f) {
+        float gs = 0.0f, us = 0.0f;
+        for (int32_t d = 0; d < D; ++d) {
+            gs += bf16_to_f32(wg[(size_t)f * D + d]) * xt[d];
+            us += bf16_to_f32(wu[(size_t)f * D + d]) * xt[d];
+        }
+        g[f] = gs;
+        u[f] = us;
+        a[f] = gs / (1.0f + expf(-gs));
+        h[f] = a[f] * us;
+    }
+    for (int32_t f = 0; f < F; ++f) w2t_dout[f] = 0.0f;
+    for (int32_t j = 0; j < D; ++j) {
+        const float dj = dout_t[j];
+        for (int32_t f = 0; f < F; ++f) w2t_dout[f] += bf16_to_f32(w2e[(size_t)j * F + f]) * dj;
+    }
+}
+
+static float silu_grad(float g) {
+    const float sig = 1.0f / (1.0f + expf(-g));
+    return sig * (1.0f + g * (1.0f - sig));
+}
+
+/* Pass A: dx[t] and dscores[t, :] for tokens t_begin .. t_end-1 (range in the forward job). */
+static void *oracle_bwd_tokens(void *arg) {
+    oracle_bwd_job *job = (oracle_bwd_job *)arg;
+    const oracle_job *fw = job->fw;
+    const int32_t D = fw->D, F = fw->F, E = fw->E, K = fw->K;
+    float *buf = (float *)malloc(sizeof(float) * ((size_t)2 * D + (size_t)7 * F));
+    if (!buf) {
+        job->failed = 1;
+        return NULL;
+    }
+    float *xt = buf, *dxt = buf + D, *g = dxt + D, *u = g + F, *a = u + F, *h = a + F, *w2t = h + F,
+          *dg = w2t + F, *du = dg + F;
+    for (int64_t t = fw->t_begin; t < fw->t_end; ++t) {
+        const float *dout_t = job->dout + t * D;
+        for (int32_t d = 0; d < D; ++d) xt[d] = bf16_to_f32(fw->x[t * D + d]);
+        for (int32_t d = 0; d < D; ++d) dxt[d] = 0.0f;
+        for (int32_t k = 0; k < K; ++k) {
+            const int32_t e = fw->ids[t * K + k];
+            job->dscores[t * K + k] = 0.0f;
+            if (e < 0 || e >= E) continue;
+            const float s = pair_score(fw, t * K + k);
+            pair_recompute(fw, xt, dout_t, e, g, u, a, h, w2t);
+            /* dscores = <dout, W2 h> = <W2^T dout, h> */
+            float ds = 0.0f;
+            for (int32_t f = 0; f < F; ++f) ds += w2t[f] * h[f];
+            job->dscores[t * K + k] = ds;
+            for (int32_t f = 0; f < F; ++f) {
+                const float dh = s * w2t[f];
+                dg[f] = dh * u[f] * silu_grad(g[f]);
+                du[f] = dh * a[f];
+            }
+            const uint16_t *wg = fw->w13 + ((size_t)e * 2 + 0) * (size_t)F * (size_t)D;
+            const uint16_t *wu = fw->w13 + ((size_t)e * 2 + 1) * (size_t)F * (size_t)D;
+            for (int32_t d = 0; d < D; ++d) {
+                float acc = 0.0f;
+                for (int32_t f = 0; f < F; ++f)
+                    acc += bf16_to_f32(wg[(size_t)f * D + d]) * dg[f] + bf16_to_f32(wu[(size_t)f * D + d]) * du[f];
+                dxt[d] += acc;
+            }
+        }
+        for (int32_t d = 0; d < D; ++d) job->dx[t * D + d] = dxt[d];
+    }
+    free(buf);
+    return NULL;
+}
+
+/* Pass B: weight gradients of experts e_begin .. e_end-1. */
+static void *oracle_bwd_experts(void *arg) {
+    oracle_bwd_job *job = (oracle_bwd_job *)arg;
+    const oracle_job *fw = job->fw;
+    const int32_t D = fw->D, F = fw->F, K = fw->K;
+    const int64_t R = fw->t_end * (int64_t)K; /* fw covers all tokens here */
+    float *buf = (float *)malloc(sizeof(float) * ((size_t)D + (size_t)7 * F));
+    if (!buf) {
+        job->failed = 1;
+        return NULL;
+    }
+    float *xt = buf, *g = xt + D, *u = g + F, *a = u + F, *h = a + F, *w2t = h + F, *dg = w2t + F, *du = dg + F;
+    for (int32_t e = job->e_begin; e < job->e_end; ++e) {
+        float *dwg = job->dw13 + ((size_t)e * 2 + 0) * (size_t)F * (size_t)D;
+        float *dwu = job->dw13 + ((size_t)e * 2 + 1) * (size_t)F * (size_t)D;
+        float *dw2e = job->dw2 + (size_t)e * (size_t)D * (size_t)F;
+        for (size_t i = 0; i < (size_t)F * D; ++i) dwg[i] = dwu[i] = 0.0f;
+        for (size_t i = 0; i < (size_t)D * F; ++i) dw2e[i] = 0.0f;
+        for (int64_t p = 0; p < R; ++p) {
+            if (fw->ids[p] != e) continue;
+            const int64_t t = p / K;
+            const float s = pair_score(fw, p);
+            const float *dout_t = job->dout + t * D;
+            for (int32_t d = 0; d < D; ++d) xt[d] = bf16_to_f32(fw->x[t * D + d]);
+            pair_recompute(fw, xt, dout_t, e, g, u, a, h, w2t);
+            for (int32_t f = 0; f < F; ++f) {
+                const float dh = s * w2t[f];
+                dg[f] = dh * u[f] * silu_grad(g[f]);
+                du[f] = dh * a[f];
+            }
+            for (int32_t j = 0; j < D; ++j) {
+                const float dy = s * dout_t[j];
+                for (int32_t f = 0; f < F; ++f) dw2e[(size_t)j * F + f] += dy * h[f];
+            }
+            for (int32_t f = 0; f < F; ++f)
+                for (int32_t d = 0; d < D; ++d) {
+                    dwg[(size_t)f * D + d] += dg[f] * xt[d];
+                    dwu[(size_t)f * D + d] += du[f] * xt[d];
+                }
+        }
+    }
+    free(buf);
+    return NULL;
+}
+
+/*
+ * Gradients of the layer for an upstream gradient dout [T,D] (fp32): dx [T,D], dscores [T,K],
+ * dw13 [E,2,F,D], dw2 [E,D,F], all fp32 and written in full. Inputs as for oracle_routed_experts.
+ * Returns 0, or -1 on a bad argument or an allocation failure.
+ */
+int oracle_routed_experts_bwd(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
+                              const uint16_t *w13, const uint16_t *w2, const float *dout, float *dx,
+                              float *dscores, float *dw13, float *dw2, int64_t T, int32_t D, int32_t F,
+                              int32_t E, int32_t K, int nthreads) {
+    if (T < 0 || D <= 0 || F <= 0 || E <= 0 || K <= 0) return -1;
+    if (nthreads < 1) nthreads = 1;
+    oracle_job *fws = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
+    oracle_bwd_job *jobs = (oracle_bwd_job *)calloc((size_t)nthreads, sizeof(oracle_bwd_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    unsigned char *running = (unsigned char *)calloc((size_t)nthreads, 1);
+    int rc = 0;
+    if (!fws || !jobs || !tids || !running) {
+        rc = -1;
+        goto done;
+    }
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int i = 0; i < nthreads; ++i) {
+            oracle_job *f = &fws[i];
+            memset(f, 0, sizeof *f);
+            f->x = x;
+            f->ids = ids;
+            f->scores = scores;
+            f->scores_bf16 = scores_bf16;
+            f->w13 = w13;
+            f->w2 = w2;
+            f->D = D;
+            f->F = F;
+            f->E = E;
+            f->K = K;
+            if (pass == 0) {
+                f->t_begin = T * i / nthreads;
+                f->t_end = T * (i + 1) / nthreads;
+            } else {
+                f->t_begin = 0;
+                f->t_end = T;
+            }
+            oracle_bwd_job *j = &jobs[i];
+            memset(j, 0, sizeof *j);
+            j->fw = f;
+            j->dout = dout;
+            j->dx = dx;
+            j->dscores = dscores;
+            j->dw13 = dw13;
+            j->dw2 = dw2;
+            j->e_begin = (int32_t)((int64_t)E * i / nthreads);
+            j->e_end = (int32_t)((int64_t)E * (i + 1) / nthreads);
+        }
+        void *(*fn)(void *) = pass == 0 ? oracle_bwd_tokens : oracle_bwd_experts;
+        for (int i = 1; i < nthreads; ++i) running[i] = (pthread_create(&tids[i], NULL, fn, &jobs[i]) == 0);
+        fn(&jobs[0]);
+        for (int i = 1; i < nthreads; ++i)
+            if (running[i]) pthread_join(tids[i], NULL);
+        for (int i = 1; i < nthreads; ++i)
+            if (!running[i]) fn(&jobs[i]);
+        for (int i = 0; i < nthreads; ++i)
+            if (jobs[i].failed) rc = -1;
+    }
+done:
+    free(fws);
+    free(jobs);
+    free(tids);
+    free(running);
     return rc;
 }

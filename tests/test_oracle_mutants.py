@@ -9,6 +9,7 @@ import os
 import pytest
 
 import oracle
+import oracle_bwd_pins
 import oracle_pins
 
 MUTANTS = {
@@ -32,6 +33,14 @@ MUTANTS = {
     "invalid_ids_kept": [("int32_t key = (e >= 0 && e < E) ? e : E;", "int32_t key = (e >= 0 && e < E) ? e : 0;")],
     "inv_identity": [("inv[i] = (int32_t)r;", "inv[i] = (int32_t)i;")],
     "round_h_truncates": [("u += 0x7fffu + ((u >> 16) & 1u);", "u += 0u;")],
+    # backward
+    "bwd_silu_grad_sign": [("return sig * (1.0f + g * (1.0f - sig));", "return sig * (1.0f - g * (1.0f - sig));")],
+    "bwd_dh_without_score": [("const float dh = s * w2t[f];", "const float dh = w2t[f];")],
+    "bwd_dw2_without_score": [("const float dy = s * dout_t[j];", "const float dy = dout_t[j];")],
+    "bwd_dx_without_up_term": [(" + bf16_to_f32(wu[(size_t)f * D + d]) * du[f];", ";")],
+    "bwd_dscore_scaled": [("ds += w2t[f] * h[f];", "ds += w2t[f] * h[f] * s;")],
+    "bwd_du_from_gate": [("du[f] = dh * a[f];", "du[f] = dh * g[f];")],
+    "bwd_dwu_from_dg": [("dwu[(size_t)f * D + d] += du[f] * xt[d];", "dwu[(size_t)f * D + d] += dg[f] * xt[d];")],
 }
 
 
@@ -48,7 +57,7 @@ def test_pins_reject_mutant(name, tmp_path):
     oracle.compile_oracle(str(path), lib_path)
     lib = oracle.load_library(lib_path)
     failed = []
-    for check in oracle_pins.ALL_PINS:
+    for check in oracle_pins.ALL_PINS + oracle_bwd_pins.BWD_PINS:
         try:
             check(lib=lib)
         except AssertionError:

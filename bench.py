@@ -50,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--config", default="medium", choices=["tiny", "medium", "decode", "large", "skewed"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                   help="fwd: the forward layer (the headline); bwd: its backward pass (one call per step)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--tokens", type=int, default=None,
                    help="replace the workload's T (smaller cases for profiling runs)")
@@ -492,6 +494,88 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------------------ backward pass
+
+def run_ours_bwd(args, rank, world, local_rank):
+    """Times moe_routed_experts_bwd: dx, dscores, dw13, dw2 for one upstream gradient per step."""
+    import torch
+
+    from mixture_experts_routed_topk_gb300 import binding, build
+    from mixture_experts_routed_topk_gb300 import workloads as W
+
+    build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+    wl = W.WORKLOADS[args.config]
+    if args.tokens:
+        wl = dataclasses.replace(wl, T=int(args.tokens))
+    T, D, F, E, K = wl.dims()
+    rseed = replica_seed(args.seed, rank)
+    x = W.make_x(T, D, rseed, device)
+    ids = W.make_topk_ids(T, E, K, wl.routing, rseed, device)
+    scores = W.make_scores(T, K, wl.scores, rseed, device)
+    dout = W.make_x(T, D, rseed + 101, device)
+    w13, w2 = W.make_weights(E, D, F, args.seed, device)
+    ws = binding.alloc_workspace(binding.moe_bwd_workspace_bytes(T, D, F, E, K), device)
+    dx = torch.empty_like(x)
+    dscores = torch.empty((T, K), dtype=torch.float32, device=device)
+    dw13, dw2 = torch.empty_like(w13), torch.empty_like(w2)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        binding.moe_routed_experts_bwd(x, ids, scores, w13, w2, dout, dx, dscores, dw13, dw2, ws, stream)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    if binding.moe_get_status(ws, stream) != 0:
+        raise RuntimeError("device status bits after warm-up")
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(device).uuid))
+    sampler.start()
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    for i in range(args.steps):
+        flush.zero_()
+        events[i][0].record(stream)
+        step()
+        events[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    sampler.stop()
+    total_s = reduce_max(dist, sum(e[0].elapsed_time(e[1]) for e in events) / 1e3)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = measured_peaks()
+    R = T * K
+    # recompute 4RDF + dgrad(down) 2RDF + dgrad(gate/up) 4RDF + wgrad(down) 2RDF + wgrad(gate/up) 4RDF
+    flops = 16 * R * D * F
+    step_s = total_s / args.steps
+    achieved = world * flops / step_s / 1e12
+    sustained = total_s > 2.0
+    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    print(assemble_line(
+        metric="routed-expert bwd tokens/s and TFLOP/s on 1 GB300; % of roofline",
+        value=round(world * T * args.steps / total_s, 1), unit="tokens/s", n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=round(step_s * 1e3, 4), higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="bf16", data="synthetic",
+        config={"workload": args.config if not args.tokens else f"{args.config} (T={T})", "T": T, "D": D, "F": F,
+                "E": E, "K": K, "routing": wl.routing, "pass": "bwd", "l2": "flushed between steps (512 MB write)"},
+        tflops=round(achieved, 2),
+        roofline={"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                  "frac": round(achieved / peak, 4), "traffic": None, "kernel": "whole backward call (16 RDF flops)",
+                  "peak_kind": "sustained" if sustained else "burst", "peak_source": peak_src},
+        gpu_launches=None, clocks=sampler.summary(), cpu_baseline=None,
+    ), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank, world, local_rank):
@@ -541,6 +625,8 @@ def main(argv=None):
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world, local_rank)
+    elif args.which == "bwd":
+        run_ours_bwd(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)
 

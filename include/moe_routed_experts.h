@@ -186,6 +186,39 @@ moe_status_t moe_fwd_combine(const int32_t *topk_ids, void *out, int64_t T, int3
                              int32_t E, int32_t K, void *workspace, size_t workspace_bytes,
                              moe_stream_t stream);
 
+/*
+ * Bytes of device workspace that moe_routed_experts_bwd needs (0 for T = 0 or sizes outside the
+ * shape limits). Pure arithmetic.
+ */
+size_t moe_bwd_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K);
+
+/*
+ * The backward pass of the layer (Dist-MoE 0.1.0, "Understand the execution model": DGRAD computes
+ * input gradients and WGRAD weight gradients; the TeraMoE README's example calls
+ * output.backward). For the upstream gradient dout of out, with e = ids[t,k], s = scores[t,k]:
+ *   dscores[t,k] = < dout[t], W2[e] (SiLU(Wg[e] x_t) * (Wu[e] x_t)) >
+ *   dx[t]        = sum_k Wg[e]^T dg + Wu[e]^T du,  dh = s W2[e]^T dout[t],
+ *                  dg = dh * (Wu[e] x_t) * SiLU'(Wg[e] x_t),  du = dh * SiLU(Wg[e] x_t)
+ *   dw2[e]       = sum over the pairs of e of (s dout[t]) h^T
+ *   dw13[e]      = sum over the pairs of e of [dg; du] x_t^T
+ * Inputs as for moe_routed_experts_fwd, plus
+ *   dout     device bf16 [T,D]
+ *   dx       device bf16 [T,D]         (written in full)
+ *   dscores  device fp32 [T,K]         (written in full; 0 for ids outside [0, E))
+ *   dw13     device bf16 [E,2,F,D]     (written in full; zero for experts with no pairs)
+ *   dw2      device bf16 [E,D,F]       (written in full)
+ *   workspace device, moe_bwd_workspace_bytes(T, D, F, E, K) bytes; its first 4 bytes are the
+ *            device status word (moe_get_status)
+ * The forward activations are recomputed (nothing from the forward call is needed). bf16
+ * operands, fp32 accumulation, bf16 intermediates; deterministic. T = 0 writes zero weight
+ * gradients.
+ */
+moe_status_t moe_routed_experts_bwd(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                    int32_t scores_dtype, const void *w13, const void *w2, const void *dout,
+                                    void *dx, float *dscores, void *dw13, void *dw2, int64_t T, int32_t D,
+                                    int32_t F, int32_t E, int32_t K, void *workspace, size_t workspace_bytes,
+                                    moe_stream_t stream);
+
 /* Capacity of the library-owned scratch of moe_routing_static_scratch, in int32 entries per
  * array: it serves sizes with (E + 1) * ceil(T*K / 2048) <= this value. */
 #define MOE_STATIC_SCRATCH_MAX_ENTRIES 262144

@@ -15,6 +15,8 @@ __all__ = [
     "moe_fwd_gemm2",
     "moe_fwd_combine",
     "moe_routed_experts_fwd",
+    "moe_bwd_workspace_bytes",
+    "moe_routed_experts_bwd",
     "moe_get_status",
     "moe_status_string",
     "MoeError",

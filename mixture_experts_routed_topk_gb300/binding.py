@@ -69,6 +69,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "moe_get_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
             "moe_routing_static_scratch": ([vp, i64, i32, i32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "moe_selftest_wait_timeout": ([ctypes.c_uint32, vp, vp], ctypes.c_int),
+            "moe_bwd_workspace_bytes": ([i64, i32, i32, i32, i32], sz),
+            "moe_routed_experts_bwd": (
+                [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
             "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -225,6 +228,36 @@ def moe_routing_static_scratch(topk_ids, num_experts: int, counts, offsets, perm
     _check("moe_routing_static_scratch", load().moe_routing_static_scratch(
         _ptr(topk_ids), T, int(num_experts), K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
         _ptr(device_status), _stream_handle(stream)))
+
+
+def moe_bwd_workspace_bytes(T: int, D: int, F: int, E: int, K: int) -> int:
+    return int(load().moe_bwd_workspace_bytes(T, D, F, E, K))
+
+
+def moe_routed_experts_bwd(x, topk_ids, topk_scores, w13, w2, dout, dx, dscores, dw13, dw2, workspace,
+                           stream=None) -> None:
+    """Gradients of the layer: dx [T,D] bf16, dscores [T,K] fp32, dw13 [E,2,F,D] and dw2 [E,D,F] bf16."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
+    _need(w13, "w13", torch.bfloat16, 4)
+    _need(w2, "w2", torch.bfloat16, 3)
+    _need(dout, "dout", torch.bfloat16, 2)
+    _need(dx, "dx", torch.bfloat16, 2)
+    _need(dscores, "dscores", torch.float32, 2)
+    _need(dw13, "dw13", torch.bfloat16, 4)
+    _need(dw2, "dw2", torch.bfloat16, 3)
+    _need(workspace, "workspace", torch.uint8)
+    T, D, F, E, K = _dims(x, topk_ids, w13)
+    for name, t, shape in (("w2", w2, (E, D, F)), ("dout", dout, (T, D)), ("dx", dx, (T, D)),
+                           ("dscores", dscores, (T, K)), ("dw13", dw13, (E, 2, F, D)), ("dw2", dw2, (E, D, F)),
+                           ("topk_scores", topk_scores, (T, K))):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {shape}, got {tuple(t.shape)}")
+    sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
+    _check("moe_routed_experts_bwd", load().moe_routed_experts_bwd(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(dout), _ptr(dx), _ptr(dscores),
+        _ptr(dw13), _ptr(dw2), T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
 
 
 def moe_selftest_wait_timeout(timeout_us: int, device_status, stream=None) -> None:

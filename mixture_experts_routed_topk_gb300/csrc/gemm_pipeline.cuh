@@ -1,0 +1,326 @@
+// gemm_pipeline.cuh -- the persistent, warp-specialised tcgen05 GEMM pipeline shared by every
+// grouped GEMM of the library (forward and backward), generic over a tile policy.
+//
+// One CTA per SM walks tiles c, c + grid, ... of a tile list the policy defines. Warp 0 issues TMA
+// loads into a 4-stage shared-memory ring (48 KB per stage: 16 KB of A, 32 KB of B), warp 1 owns
+// all 512 TMEM columns and issues tcgen05.mma from one thread into one of two 128 x 256 fp32
+// accumulators, warps 2-5 run the policy's epilogue from TMEM (one TMEM lane = one output row
+// per thread). full/empty mbarriers link producer and MMA; acc_full/acc_empty link MMA and
+// epilogue, so a tile's epilogue overlaps the next tile's mainloop. Every wait is bounded.
+//
+// A policy P provides
+//   struct P::Tile { int32_t kblocks; ... }              one tile's coordinates and K steps
+//   static constexpr uint32_t kIdesc                     tcgen05 instruction descriptor
+//   static constexpr bool kAMnMajor, kBMnMajor           operand layouts in shared memory
+//   __device__ static int32_t num_tiles(const GemmArgs&)
+//   __device__ static Tile decode(int32_t tile, const GemmArgs&)
+//   __device__ static void load(const Tile&, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
+//                               const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs&)
+//   __device__ static void epilogue(const Tile&, uint32_t taddr, int row, uint4* stage,
+//                                   const GemmArgs&)          (taddr = this warp's TMEM lanes)
+// Every load() must deliver exactly kStageBytes into the stage.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "moe_internal.cuh"
+#include "ptx_sm103.cuh"
+
+namespace moe {
+
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;      // 16 KB: 128 rows x 64 bf16
+constexpr int kBRows = 256;                 // accumulator columns per tile
+constexpr int kBBytes = kBRows * kBK * 2;   // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kAccCols = 256;
+constexpr int kTmemCols = 512;
+constexpr int kGemmThreads = 192;
+constexpr int kEpilogueThreads = 128;
+constexpr int kMnBoxBytes = 64 * kBK * 2;   // one 64 (M or N) x 64 (K) MN-major box: 8 KB
+
+// Epilogue staging: each epilogue warp owns 32 rows x 128 bytes (+16 bytes of padding per row, so
+// that both the per-thread row writes and the per-row reads are free of bank conflicts).
+constexpr int kStageRowU4 = 9;  // 144-byte row stride in 16-byte units
+constexpr int kEpilogueStagingBytes = (kEpilogueThreads / 32) * 32 * kStageRowU4 * 16;
+
+struct alignas(8) PipeState {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kGemmSmemBytes =
+    1024 + static_cast<size_t>(kStages) * kStageBytes + kEpilogueStagingBytes + sizeof(PipeState);
+
+// Everything any policy needs (each policy reads its own fields).
+struct GemmArgs {
+    const int32_t* counts;   // [E] routed rows per expert
+    const int32_t* offsets;  // [E+1] first routed row per expert
+    const int32_t* tiles;    // [E+1] forward tile prefix
+    const int32_t* pmt;      // [E+1] padded 128-row tile prefix (backward)
+    const int32_t* perm;     // routed row -> pair
+    const int32_t* pperm;    // padded row -> pair, or -1 (backward)
+    int32_t E;
+    int32_t kblocks;         // K extent / 64 for fixed-K policies
+    int32_t D, F;
+    int32_t mdim, ndim;      // weight-gradient output rows / columns
+    int32_t mtiles, ntiles;  // weight-gradient tile grid per expert
+    const void* scores;      // [T*K] fp32 or bf16
+    int32_t scores_bf16;
+    __nv_bfloat16* out0;     // policy output 1
+    __nv_bfloat16* out1;     // policy output 2
+    const __nv_bfloat16* in0;  // extra epilogue input
+    float* fout;             // fp32 policy output
+    uint32_t* status;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float pair_score(const GemmArgs& a, int32_t pair) {
+    return a.scores_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.scores)[pair])
+                         : __ldg(reinterpret_cast<const float*>(a.scores) + pair);
+}
+
+// The expert owning `tile` in a tile list whose prefix is ntn * prefix[e]: the last e with
+// ntn * prefix[e] <= tile.
+__device__ __forceinline__ int32_t owning_expert(int32_t tile, const int32_t* prefix, int32_t ntn, int32_t E) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ntn * __ldg(prefix + mid) <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast, so tcgen05.ld (which needs
+// the whole warp) is executed by all lanes or none.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status, MOE_DEV_TIMEOUT) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Writes, for every lane of the warp, 64 bf16 (128 bytes, packed two per 32-bit word) to that
+// lane's own row. Lane i's words go to its staging row first; then lane l copies 16-byte piece
+// (l & 7) of row (4 j + l / 8) for j = 0..7, so one store instruction covers four complete
+// 128-byte row segments. dst: this lane's destination (16-byte aligned); ok: whether this lane's
+// row is stored at all.
+__device__ __forceinline__ void warp_store_row_segments(uint4* stage, const uint32_t (&words)[32], char* dst,
+                                                        bool ok) {
+    const int lane = threadIdx.x & 31;
+    uint4* mine = stage + lane * kStageRowU4;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        mine[c] = make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+    __syncwarp();
+    const unsigned long long my_dst = reinterpret_cast<unsigned long long>(dst);
+    const int my_ok = ok ? 1 : 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int r = 4 * j + (lane >> 3);
+        const int piece = lane & 7;
+        const unsigned long long rd = __shfl_sync(0xffffffffu, my_dst, r);
+        const int rok = __shfl_sync(0xffffffffu, my_ok, r);
+        if (rok) reinterpret_cast<uint4*>(rd)[piece] = stage[r * kStageRowU4 + piece];
+    }
+    __syncwarp();
+}
+
+// 16 packed words (32 bf16 = 64 bytes) to a 16-byte-aligned address.
+__device__ __forceinline__ void store_64B(void* dst, const uint32_t (&w)[16]) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+// Shared-memory operand descriptor of the 16-wide K step kk of a stage operand at `base`.
+template <bool kMnMajor>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
+    // K-major: each K step is 32 bytes further along the swizzled 128-byte rows.
+    // MN-major: each K step is 16 rows of 128 bytes further down the 64-wide MN blocks.
+    return kMnMajor ? sw128_mnmajor_desc(base + kk * 2048, kMnBoxBytes) : sw128_kmajor_desc(base + kk * 32);
+}
+
+template <class P>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_grouped_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared address space
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    uint4* staging = reinterpret_cast<uint4*>(smem + kStages * kStageBytes);
+    PipeState* ps = reinterpret_cast<PipeState*>(smem + kStages * kStageBytes + kEpilogueStagingBytes);
+    volatile int* abort_flag = &ps->abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ps->full[s], 1);
+            mbar_init(&ps->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ps->acc_full[b], 1);
+            mbar_init(&ps->acc_empty[b], kEpilogueThreads);
+        }
+        mbar_init(&ps->drain, 1);
+        ps->abort = 0;
+        mbar_init_fence();
+        tma_prefetch_descriptor(&tmap_a);
+        tma_prefetch_descriptor(&tmap_b);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(&ps->tmem_base, kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tcgen05_fence_before_sync();
+    __syncthreads();
+    tcgen05_fence_after_sync();
+    // everything above overlaps the previous kernel's tail; its outputs are read from here on
+    griddep_wait();
+    griddep_launch_dependents();
+    const uint32_t tmem_base = ps->tmem_base;
+    const int32_t total = P::num_tiles(args);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int32_t tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                const typename P::Tile t = P::decode(tile, args);
+                for (int32_t kb = 0; kb < t.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!mbar_wait(&ps->empty[s], ph ^ 1u, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + s * kStageBytes;
+                    mbar_arrive_expect_tx(&ps->full[s], kStageBytes);
+                    P::load(t, kb, sa, sa + kABytes, &ps->full[s], &tmap_a, &tmap_b, args);
+                }
+            }
+            if (!ok) {
+                // aborting: give the copies already issued time to land before the CTA exits
+                const unsigned long long t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, tcount = 0;
+            bool ok = true;
+            for (int32_t tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tcount) {
+                const typename P::Tile t = P::decode(tile, args);
+                const uint32_t acc = tcount & 1u;
+                const uint32_t aph = (tcount >> 1) & 1u;
+                if (!mbar_wait(&ps->acc_empty[acc], aph ^ 1u, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                tcgen05_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * kAccCols;
+                for (int32_t kb = 0; kb < t.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!mbar_wait(&ps->full[s], ph, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_fence_after_sync();
+                    const uint32_t a0 = smem_addr(smem + s * kStageBytes);
+                    const uint32_t b0 = a0 + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16_ss(d_tmem, operand_desc<P::kAMnMajor>(a0, kk), operand_desc<P::kBMnMajor>(b0, kk),
+                                    P::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    mma_commit(&ps->empty[s]);  // frees the stage once these MMAs have read it
+                }
+                if (!ok) break;
+                mma_commit(&ps->acc_full[acc]);  // a tile without K steps signals at once
+            }
+            if (!ok) {
+                // aborting: wait (bounded) until every MMA issued so far has finished with TMEM
+                mma_commit(&ps->drain);
+                const unsigned long long t0 = global_timer_ns();
+                while (!mbar_try_wait(&ps->drain, 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue (warps 2-5)
+        const int quarter = warp & 3;  // TMEM lanes this warp may access: 32*quarter .. +31
+        const int row_in_tile = quarter * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        uint4* wstage = staging + (warp - 2) * 32 * kStageRowU4;
+        uint32_t tcount = 0;
+        for (int32_t tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
+            const typename P::Tile t = P::decode(tile, args);
+            const uint32_t acc = tcount & 1u;
+            const uint32_t aph = (tcount >> 1) & 1u;
+            if (!warp_wait(&ps->acc_full[acc], aph, abort_flag, args.status)) break;
+            tcgen05_fence_after_sync();
+            P::epilogue(t, tmem_base + lane_base + acc * kAccCols, row_in_tile, wstage, args);
+            tcgen05_fence_before_sync();
+            mbar_arrive(&ps->acc_empty[acc]);
+        }
+    }
+
+    tcgen05_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();  // lane 0 ran the MMA loop alone; .sync.aligned needs the whole warp
+        tcgen05_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------------------- host
+
+// A 2-D bf16 tensor [rows, inner] (inner contiguous) read in boxes of box_inner x box_rows with
+// 128-byte swizzle; reads outside the tensor return zeros.
+bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+               uint32_t box_rows);
+
+int sm_count_grid(int64_t max_tiles, int sm_count);
+
+template <class P>
+moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
+                         cudaStream_t stream) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<bool> attr_set[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(k_grouped_gemm<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGemmSmemBytes)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set[dev].store(true, std::memory_order_release);
+    }
+    return launch_pdl(k_grouped_gemm<P>, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, stream, ta, tb, a) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

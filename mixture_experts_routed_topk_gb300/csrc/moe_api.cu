@@ -185,6 +185,69 @@ moe_status_t do_combine(const Call& c, const int32_t* ids, void* out, int64_t T,
 
 bool bad_scores_dtype(int32_t d) { return d != MOE_SCORES_F32 && d != MOE_SCORES_BF16; }
 
+// Backward workspace: routing arrays, the padded-row maps and the padded activation buffers.
+enum {
+    BW_STATUS,
+    BW_COUNTS,
+    BW_OFFSETS,
+    BW_BLOCK_COUNTS,
+    BW_BLOCK_BASES,
+    BW_PERM,
+    BW_INV,
+    BW_PMT,
+    BW_PPERM,
+    BW_PINV,
+    BW_XPP,
+    BW_DOP,
+    BW_GU,
+    BW_HS,
+    BW_DGU,
+    BW_PARTIAL,
+    BW_DXP,
+    BW_TOTAL
+};
+
+struct BwdLayout {
+    size_t off[BW_TOTAL + 1];
+    int nblk;
+    int64_t padded_rows;
+};
+
+bool make_bwd_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, BwdLayout* L) {
+    if (check_shape(T, D, F, E, K, true) != MOE_OK || T == 0) return false;
+    const int64_t R = T * static_cast<int64_t>(K);
+    const int64_t nonempty = R < E ? R : E;
+    L->padded_rows = ceil_div(R + 127 * nonempty, 128) * 128;
+    if (L->padded_rows >= (int64_t{1} << 31)) return false;
+    L->nblk = static_cast<int>(ceil_div(R, kRouteChunk));
+    const size_t e1 = static_cast<size_t>(E) + 1, rp = static_cast<size_t>(L->padded_rows);
+    size_t sizes[BW_TOTAL] = {};
+    sizes[BW_STATUS] = sizeof(uint32_t);
+    sizes[BW_COUNTS] = sizeof(int32_t) * E;
+    sizes[BW_OFFSETS] = sizeof(int32_t) * e1;
+    sizes[BW_BLOCK_COUNTS] = sizeof(int32_t) * e1 * L->nblk;
+    sizes[BW_BLOCK_BASES] = sizeof(int32_t) * e1 * L->nblk;
+    sizes[BW_PERM] = sizeof(int32_t) * R;
+    sizes[BW_INV] = sizeof(int32_t) * R;
+    sizes[BW_PMT] = sizeof(int32_t) * e1;
+    sizes[BW_PPERM] = sizeof(int32_t) * rp;
+    sizes[BW_PINV] = sizeof(int32_t) * R;
+    sizes[BW_XPP] = 2 * rp * D;
+    sizes[BW_DOP] = 2 * rp * D;
+    sizes[BW_GU] = 2 * rp * 2 * F;
+    sizes[BW_HS] = 2 * rp * F;
+    sizes[BW_DGU] = 2 * rp * 2 * F;
+    sizes[BW_PARTIAL] = sizeof(float) * rp * ceil_div(F, kBN2);
+    sizes[BW_DXP] = 2 * rp * D;
+    size_t off = 0;
+    for (int r = 0; r < BW_TOTAL; ++r) {
+        L->off[r] = off;
+        off += align_up(sizes[r]);
+    }
+    L->off[BW_TOTAL] = off;
+    return true;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -312,6 +375,83 @@ moe_status_t moe_routed_experts_fwd(const void* x, const int32_t* topk_ids, cons
     if ((st = do_gemm1(c, w13, D, F, E, s)) != MOE_OK) return st;
     if ((st = do_gemm2(c, topk_scores, scores_dtype, w2, D, F, E, s)) != MOE_OK) return st;
     return do_combine(c, topk_ids, out, T, D, E, K, s);
+}
+
+size_t moe_bwd_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K) {
+    BwdLayout L;
+    if (!make_bwd_layout(T, D, F, E, K, &L)) return 0;
+    return L.off[BW_TOTAL];
+}
+
+moe_status_t moe_routed_experts_bwd(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                    int32_t scores_dtype, const void* w13, const void* w2, const void* dout, void* dx,
+                                    float* dscores, void* dw13, void* dw2, int64_t T, int32_t D, int32_t F, int32_t E,
+                                    int32_t K, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    if (bad_scores_dtype(scores_dtype)) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, D, F, E, K, true);
+    if (st != MOE_OK) return st;
+    if (!w13 || !w2 || !dw13 || !dw2) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w13, 16) || !aligned(w2, 16) || !aligned(dw13, 16) || !aligned(dw2, 16)) return MOE_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeviceInfo dev;
+    if (T == 0) {
+        // no tokens: the weight gradients are zero
+        if ((st = device_info(&dev)) != MOE_OK) return st;
+        if (cudaMemsetAsync(dw13, 0, 2ull * E * 2 * F * D, s) != cudaSuccess ||
+            cudaMemsetAsync(dw2, 0, 2ull * E * D * F, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (!x || !topk_ids || !topk_scores || !dout || !dx || !dscores || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(dout, 16) || !aligned(dx, 16) || !aligned(topk_ids, 4) || !aligned(dscores, 4) ||
+        !aligned(topk_scores, scores_dtype == MOE_SCORES_F32 ? 4 : 2))
+        return MOE_ERR_MISALIGNED;
+    if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;
+    BwdLayout L;
+    if (!make_bwd_layout(T, D, F, E, K, &L)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (workspace_bytes < L.off[BW_TOTAL]) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((st = device_info(&dev)) != MOE_OK) return st;
+    if (!dev.supported) return MOE_ERR_UNSUPPORTED_DEVICE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    auto at = [&](int r) { return ws + L.off[r]; };
+    BwdProblem p{};
+    p.T = T;
+    p.D = D;
+    p.F = F;
+    p.E = E;
+    p.K = K;
+    p.x = x;
+    p.ids = topk_ids;
+    p.scores = topk_scores;
+    p.scores_dtype = scores_dtype;
+    p.w13 = w13;
+    p.w2 = w2;
+    p.dout = dout;
+    p.dx = dx;
+    p.dscores = dscores;
+    p.dw13 = dw13;
+    p.dw2 = dw2;
+    p.status = reinterpret_cast<uint32_t*>(at(BW_STATUS));
+    p.counts = reinterpret_cast<int32_t*>(at(BW_COUNTS));
+    p.offsets = reinterpret_cast<int32_t*>(at(BW_OFFSETS));
+    p.block_counts = reinterpret_cast<int32_t*>(at(BW_BLOCK_COUNTS));
+    p.block_bases = reinterpret_cast<int32_t*>(at(BW_BLOCK_BASES));
+    p.perm = reinterpret_cast<int32_t*>(at(BW_PERM));
+    p.inv = reinterpret_cast<int32_t*>(at(BW_INV));
+    p.pmt = reinterpret_cast<int32_t*>(at(BW_PMT));
+    p.pperm = reinterpret_cast<int32_t*>(at(BW_PPERM));
+    p.pinv = reinterpret_cast<int32_t*>(at(BW_PINV));
+    p.xpp = at(BW_XPP);
+    p.dop = at(BW_DOP);
+    p.gu = at(BW_GU);
+    p.hs = at(BW_HS);
+    p.dgu = at(BW_DGU);
+    p.partial = reinterpret_cast<float*>(at(BW_PARTIAL));
+    p.dxp = at(BW_DXP);
+    p.nblk = L.nblk;
+    p.padded_rows = L.padded_rows;
+    p.sm_count = dev.sm_count;
+    return launch_backward(p, s);
 }
 
 moe_status_t moe_get_status(const void* workspace, uint32_t* device_bits, moe_stream_t stream) {

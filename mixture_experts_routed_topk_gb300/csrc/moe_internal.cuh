@@ -101,6 +101,34 @@ moe_status_t launch_gemm1_swiglu(const GemmProblem& p, const void* xp, const voi
 moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void* w2, const int32_t* perm,
                                 const void* scores, int32_t scores_dtype, void* y, cudaStream_t stream);
 
+// Backward pass (backward.cu): every pointer is device memory; padded_rows is the capacity of the
+// padded-row buffers (R + 127 * min(E, R), a multiple of 128).
+struct BwdProblem {
+    int64_t T;
+    int32_t D, F, E, K;
+    const void* x;
+    const int32_t* ids;
+    const void* scores;
+    int32_t scores_dtype;
+    const void* w13;
+    const void* w2;
+    const void* dout;
+    void* dx;
+    float* dscores;
+    void* dw13;
+    void* dw2;
+    // workspace
+    uint32_t* status;
+    int32_t *counts, *offsets, *block_counts, *block_bases, *perm, *inv;
+    int32_t *pmt, *pperm, *pinv;
+    void *xpp, *dop, *gu, *hs, *dgu, *dxp;
+    float* partial;
+    int nblk;
+    int64_t padded_rows;
+    int sm_count;
+};
+moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream);
+
 moe_status_t launch_combine(const void* y, const int32_t* ids, int64_t T, int32_t D, int32_t E, int32_t K,
                             void* out, int sm_count, cudaStream_t stream);
 

@@ -150,12 +150,28 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// The same for an MN-major operand tile (M or N contiguous), as TMA writes it from boxes of
+// 64 (M or N) x rows-of-K with 128-byte swizzling: each box is a column of 8-row swizzle atoms
+// (one K row = 64 M/N values = 128 bytes). Canonical layout ((64, m), (8, k)): the leading-
+// dimension byte offset is the distance between 64-wide M/N blocks (one box, mn_block_bytes), the
+// stride-dimension byte offset the distance between 8-row K groups (1024 bytes).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma .kind::f16: D fp32 (bits [4,6) = 1), A and B bf16
-// (bits [7,10) and [10,13) = 1), both K-major (bits 15, 16 = 0), N >> 3 at [17,23), M >> 4 at
-// [24,29).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
+// (bits [7,10) and [10,13) = 1), A / B major-ness at bits 15 / 16 (0 = K-major, 1 = MN-major),
+// N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major = false,
+                                                      bool b_mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T for one M x N x 16 step, issued by a single thread.

@@ -147,6 +147,7 @@ def kernel_source_hash() -> str:
     """Hash of the grouped-GEMM sources; a recorded DRAM traffic is only valid for this hash."""
     h = hashlib.sha256()
     for rel in ("mixture_experts_routed_topk_gb300/csrc/grouped_gemm.cu",
+                "mixture_experts_routed_topk_gb300/csrc/gemm_pipeline.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/ptx_sm103.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/routing.cu",
                 "mixture_experts_routed_topk_gb300/csrc/combine.cu"):

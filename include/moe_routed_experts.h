@@ -83,8 +83,9 @@ enum {
                                 the same bytes hold Y [T, K, D], the score-weighted expert
                                 outputs per pair                                              */
     MOE_WS_H = 10,           /* bf16 [T*K, F] SwiGLU output per routed row                     */
-    MOE_WS_TOTAL = 11,       /* total bytes (== moe_workspace_bytes)                          */
-    MOE_WS_REGIONS = 12
+    MOE_WS_RMS = 11,         /* fp32 [T*K, ceil(D/256)] per-tile sums of squares (RMSNorm mode) */
+    MOE_WS_TOTAL = 12,       /* total bytes (== moe_workspace_bytes)                          */
+    MOE_WS_REGIONS = 13
 };
 
 /*
@@ -149,6 +150,20 @@ moe_status_t moe_routed_experts_fwd(const void *x, const int32_t *topk_ids, cons
                                     int32_t scores_dtype, const void *w13, const void *w2, void *out,
                                     int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
                                     void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * The forward pass with Dist-MoE's typed post-expert processing (Dist-MoE 0.1.0, "Use advanced
+ * features / Post-expert processing": route-wise RMSNorm, router-score weighting and top-k
+ * reduction fused):
+ *     out[t] = sum_k score[t,k] * y / sqrt(mean_d(y^2) + eps),   y = W2[e] (SiLU(Wg[e] x_t) * Wu[e] x_t)
+ * The norm has no gain vector (the page names only eps and the dtypes); it is taken in fp32 from
+ * the fp32 accumulator, and the weighted sum is fp32 in k order, rounded once to bf16. Arguments
+ * and workspace as for moe_routed_experts_fwd, plus eps >= 0 (MOE_ERR_INVALID_ARG otherwise).
+ */
+moe_status_t moe_routed_experts_fwd_rmsnorm(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                            int32_t scores_dtype, const void *w13, const void *w2, void *out,
+                                            int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, float eps,
+                                            void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
  * Stage 1 of the forward pass: clears the status word, routes the pairs into the workspace's

@@ -15,6 +15,7 @@ __all__ = [
     "moe_fwd_gemm2",
     "moe_fwd_combine",
     "moe_routed_experts_fwd",
+    "moe_routed_experts_fwd_rmsnorm",
     "moe_bwd_workspace_bytes",
     "moe_routed_experts_bwd",
     "moe_get_status",

@@ -25,7 +25,7 @@ MOE_DEV_TIMEOUT = 2
 
 WS_REGIONS = (
     "status", "counts", "offsets", "tiles1", "tiles2", "block_counts", "block_bases",
-    "perm", "inv", "xp", "h", "total",
+    "perm", "inv", "xp", "h", "rms", "total",
 )
 
 _lock = threading.Lock()
@@ -62,6 +62,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "moe_routing": ([vp, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "moe_routed_experts_fwd": (
                 [vp, vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_routed_experts_fwd_rmsnorm": (
+                [vp, vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, ctypes.c_float, vp, sz, vp], ctypes.c_int),
             "moe_fwd_dispatch": ([vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
             "moe_fwd_gemm1": ([vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
             "moe_fwd_gemm2": ([vp, i32, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
@@ -175,6 +177,25 @@ def moe_routed_experts_fwd(x, topk_ids, topk_scores, w13, w2, out, workspace, st
     _check("moe_routed_experts_fwd", load().moe_routed_experts_fwd(
         _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(out),
         T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_routed_experts_fwd_rmsnorm(x, topk_ids, topk_scores, w13, w2, out, workspace, eps: float = 1e-6,
+                                   stream=None) -> None:
+    """The forward pass with route-wise RMSNorm of each expert output before the score weighting."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
+    _need(w13, "w13", torch.bfloat16, 4)
+    _need(w2, "w2", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 2)
+    _need(workspace, "workspace", torch.uint8)
+    T, D, F, E, K = _dims(x, topk_ids, w13)
+    if tuple(w2.shape) != (E, D, F) or tuple(out.shape) != (T, D) or tuple(topk_scores.shape) != (T, K):
+        raise ValueError("inconsistent shapes among w2 [E,D,F], out [T,D], topk_scores [T,K]")
+    sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
+    _check("moe_routed_experts_fwd_rmsnorm", load().moe_routed_experts_fwd_rmsnorm(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(out),
+        T, D, F, E, K, float(eps), _ptr(workspace), workspace.numel(), _stream_handle(stream)))
 
 
 def moe_fwd_dispatch(x, topk_ids, dims, workspace, stream=None) -> None:

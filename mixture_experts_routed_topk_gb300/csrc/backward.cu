@@ -246,22 +246,40 @@ struct BwdDgradDown {
         const int64_t row = static_cast<int64_t>(t.row0) + row_in_tile;
         const int32_t pair = __ldg(a.pperm + row);
         const float s = pair >= 0 ? pair_score(a, pair) : 0.0f;
-        const __nv_bfloat16* gu = a.in0 + row * 2 * a.F;
+        // this row's g and u for the tile's f range, 32 values (4 x 16 bytes) per chunk; the next
+        // chunk's loads are issued before the current chunk is computed, so only the first
+        // chunk's DRAM latency is exposed
+        const uint4* grow = reinterpret_cast<const uint4*>(a.in0 + row * 2 * a.F + t.n * kBN2);
+        const uint4* urow = reinterpret_cast<const uint4*>(a.in0 + row * 2 * a.F + a.F + t.n * kBN2);
+        const int32_t nchunks = min(kBN2, a.F - t.n * kBN2) / 32;  // chunks inside F (F % 64 == 0)
+        uint4 gc[4], uc[4], gn[4], un[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            gc[v] = __ldg(grow + v);
+            uc[v] = __ldg(urow + v);
+        }
         float partial = 0.0f;
 #pragma unroll 1
         for (int c = 0; c < kBN2 / 32; ++c) {
             __syncwarp();
             uint32_t q[32];
             tmem_ld_32cols(taddr + c * 32, q);
+            if (c + 1 < nchunks) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    gn[v] = __ldg(grow + 4 * (c + 1) + v);
+                    un[v] = __ldg(urow + 4 * (c + 1) + v);
+                }
+            }
             tmem_ld_wait(q);
-            const int32_t f0 = t.n * kBN2 + c * 32;
-            if (f0 < a.F) {
+            if (c < nchunks) {
+                const int32_t f0 = t.n * kBN2 + c * 32;
                 uint32_t wdg[16], wdu[16];
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     float gg[8], uu[8];
-                    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(gu + f0) + v), gg);
-                    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(gu + a.F + f0) + v), uu);
+                    unpack_bf16x8(gc[v], gg);
+                    unpack_bf16x8(uc[v], uu);
 #pragma unroll
                     for (int i = 0; i < 8; i += 2) {
                         float dg2[2], du2[2];
@@ -281,6 +299,11 @@ struct BwdDgradDown {
                 }
                 store_64B(a.out0 + row * 2 * a.F + f0, wdg);
                 store_64B(a.out0 + row * 2 * a.F + a.F + f0, wdu);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                gc[v] = gn[v];
+                uc[v] = un[v];
             }
         }
         a.fout[row * ntn(a) + t.n] = partial;

@@ -90,7 +90,10 @@ struct FwdGateUp {
 };
 
 // Down GEMM with the score: A = H rows (K-major, K = F), B = W2 rows (K-major); Y[perm[r]] rows.
-struct FwdDown {
+// With kRms (route-wise RMSNorm post-processing) it writes the unweighted expert output instead,
+// plus each row's fp32 sum of squares over the tile's columns to fout[pair * column tiles + n].
+template <bool kRms>
+struct FwdDownT {
     using Tile = RowTile;
     static constexpr bool kAMnMajor = false, kBMnMajor = false;
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBRows);
@@ -111,8 +114,9 @@ struct FwdDown {
         float score = 0.0f;
         if (valid) {
             pair = __ldg(a.perm + row);
-            score = pair_score(a, pair);
+            score = kRms ? 1.0f : pair_score(a, pair);
         }
+        float sumsq = 0.0f;
         uint32_t words[32];  // 64 bf16 of this thread's row: two 32-column chunks
 #pragma unroll 1
         for (int cp = 0; cp < kBN2 / 64; ++cp) {
@@ -126,12 +130,17 @@ struct FwdDown {
                 for (int j = 0; j < 16; ++j)
                     words[half * 16 + j] =
                         pack_bf16x2(__uint_as_float(v[2 * j]) * score, __uint_as_float(v[2 * j + 1]) * score);
+                if (kRms && t.n * kBN2 + cp * 64 < a.D) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sumsq += __uint_as_float(v[j]) * __uint_as_float(v[j]);
+                }
             }
             const int32_t d0 = t.n * kBN2 + cp * 64;  // D % 64 == 0: the 64 columns are all in or all out
             warp_store_row_segments(stage, words,
                                     reinterpret_cast<char*>(a.out0 + static_cast<int64_t>(pair) * a.D + d0),
                                     valid && d0 < a.D);
         }
+        if (kRms && valid) a.fout[static_cast<int64_t>(pair) * ((a.D + kBN2 - 1) / kBN2) + t.n] = sumsq;
     }
 };
 
@@ -204,7 +213,8 @@ moe_status_t launch_gemm1_swiglu(const GemmProblem& p, const void* xp, const voi
 }
 
 moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void* w2, const int32_t* perm,
-                                const void* scores, int32_t scores_dtype, void* y, cudaStream_t stream) {
+                                const void* scores, int32_t scores_dtype, void* y, float* rms_sumsq,
+                                cudaStream_t stream) {
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, h, static_cast<uint64_t>(p.F), static_cast<uint64_t>(p.R), kBK, kBM) ||
         !make_tmap(&tb, w2, static_cast<uint64_t>(p.F), static_cast<uint64_t>(p.E) * p.D, kBK, kBN2))
@@ -214,7 +224,10 @@ moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void*
     a.scores = scores;
     a.scores_bf16 = scores_dtype == MOE_SCORES_BF16 ? 1 : 0;
     a.out0 = static_cast<__nv_bfloat16*>(y);
-    return launch_gemm<FwdDown>(ta, tb, a, row_grid(p, static_cast<int32_t>(ceil_div(p.D, kBN2))), stream);
+    a.fout = rms_sumsq;
+    const int grid = row_grid(p, static_cast<int32_t>(ceil_div(p.D, kBN2)));
+    return rms_sumsq ? launch_gemm<FwdDownT<true>>(ta, tb, a, grid, stream)
+                     : launch_gemm<FwdDownT<false>>(ta, tb, a, grid, stream);
 }
 
 }  // namespace moe

@@ -61,6 +61,7 @@ bool make_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool wit
         sizes[MOE_WS_INV] = sizeof(int32_t) * R;
         sizes[MOE_WS_XP] = 2 * static_cast<size_t>(R) * D;
         sizes[MOE_WS_H] = 2 * static_cast<size_t>(R) * F;
+        sizes[MOE_WS_RMS] = sizeof(float) * static_cast<size_t>(R) * ceil_div(D, kBN2);
     }
     size_t off = 0;
     for (int r = 0; r < MOE_WS_TOTAL; ++r) {
@@ -175,7 +176,7 @@ moe_status_t do_gemm2(const Call& c, const void* scores, int32_t scores_dtype, c
                       int32_t E, cudaStream_t stream) {
     return launch_gemm2_score(gemm_problem(c, D, F, E, 2), region<void>(c, MOE_WS_H), w2,
                               region<int32_t>(c, MOE_WS_PERM), scores, scores_dtype, region<void>(c, MOE_WS_XP),
-                              stream);
+                              nullptr, stream);
 }
 
 moe_status_t do_combine(const Call& c, const int32_t* ids, void* out, int64_t T, int32_t D, int32_t E, int32_t K,
@@ -452,6 +453,31 @@ moe_status_t moe_routed_experts_bwd(const void* x, const int32_t* topk_ids, cons
     p.padded_rows = L.padded_rows;
     p.sm_count = dev.sm_count;
     return launch_backward(p, s);
+}
+
+moe_status_t moe_routed_experts_fwd_rmsnorm(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                            int32_t scores_dtype, const void* w13, const void* w2, void* out,
+                                            int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, float eps,
+                                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Call c{};
+    if (bad_scores_dtype(scores_dtype) || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = prepare(T, D, F, E, K, workspace, workspace_bytes, &c);
+    if (st != MOE_OK || T == 0) return st;
+    if (!x || !topk_ids || !topk_scores || !w13 || !w2 || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) ||
+        !aligned(topk_scores, scores_dtype == MOE_SCORES_F32 ? 4 : 2))
+        return MOE_ERR_MISALIGNED;
+    if ((st = check_device(&c)) != MOE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = do_dispatch(c, x, topk_ids, D, F, E, K, s)) != MOE_OK) return st;
+    if ((st = do_gemm1(c, w13, D, F, E, s)) != MOE_OK) return st;
+    float* sumsq = region<float>(c, MOE_WS_RMS);
+    if ((st = launch_gemm2_score(gemm_problem(c, D, F, E, 2), region<void>(c, MOE_WS_H), w2,
+                                 region<int32_t>(c, MOE_WS_PERM), topk_scores, scores_dtype, region<void>(c, MOE_WS_XP),
+                                 sumsq, s)) != MOE_OK)
+        return st;
+    return launch_combine_rmsnorm(region<void>(c, MOE_WS_XP), topk_ids, topk_scores, scores_dtype, sumsq, T, D, E, K,
+                                  eps, out, c.dev.sm_count, s);
 }
 
 moe_status_t moe_get_status(const void* workspace, uint32_t* device_bits, moe_stream_t stream) {

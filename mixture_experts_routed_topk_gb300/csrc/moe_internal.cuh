@@ -98,8 +98,11 @@ struct GemmProblem {
 };
 moe_status_t launch_gemm1_swiglu(const GemmProblem& p, const void* xp, const void* w13, void* h,
                                  cudaStream_t stream);
+// rms_sumsq: null for the plain layer; otherwise the route-wise RMSNorm variant (unweighted Y
+// plus per-tile sums of squares, [T*K, ceil(D/256)] fp32).
 moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void* w2, const int32_t* perm,
-                                const void* scores, int32_t scores_dtype, void* y, cudaStream_t stream);
+                                const void* scores, int32_t scores_dtype, void* y, float* rms_sumsq,
+                                cudaStream_t stream);
 
 // Backward pass (backward.cu): every pointer is device memory; padded_rows is the capacity of the
 // padded-row buffers (R + 127 * min(E, R), a multiple of 128).
@@ -131,5 +134,10 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream);
 
 moe_status_t launch_combine(const void* y, const int32_t* ids, int64_t T, int32_t D, int32_t E, int32_t K,
                             void* out, int sm_count, cudaStream_t stream);
+
+// The combine of the route-wise RMSNorm variant: out[t] = sum_k s * y / sqrt(mean(y^2) + eps).
+moe_status_t launch_combine_rmsnorm(const void* y, const int32_t* ids, const void* scores, int32_t scores_dtype,
+                                    float* sumsq, int64_t T, int32_t D, int32_t E, int32_t K, float eps, void* out,
+                                    int sm_count, cudaStream_t stream);
 
 }  // namespace moe

@@ -58,6 +58,12 @@ def load_library(path: str) -> ctypes.CDLL:
         ctypes.c_int, ctypes.c_int,
     ]
     lib.oracle_routed_experts.restype = ctypes.c_int
+    lib.oracle_routed_experts_rmsnorm.argtypes = [
+        p, p, p, ctypes.c_int, p, p, p,
+        ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_float, ctypes.c_int,
+    ]
+    lib.oracle_routed_experts_rmsnorm.restype = ctypes.c_int
     lib.oracle_routed_experts_bwd.argtypes = [
         p, p, p, ctypes.c_int, p, p, p, p, p, p, p,
         ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
@@ -131,6 +137,29 @@ def routed_experts(x_bits, topk_ids, topk_scores, w13_bits, w2_bits, round_h: bo
     )
     if rc != 0:
         raise RuntimeError("oracle_routed_experts failed")
+    return out
+
+
+def routed_experts_rmsnorm(x_bits, topk_ids, topk_scores, w13_bits, w2_bits, eps: float,
+                           nthreads: int | None = None, lib=None) -> np.ndarray:
+    """out[T,D] (fp32) with route-wise RMSNorm of each expert output before the score weighting."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    w13 = np.ascontiguousarray(w13_bits, dtype=np.uint16)
+    w2 = np.ascontiguousarray(w2_bits, dtype=np.uint16)
+    sc = np.asarray(topk_scores)
+    scores_bf16 = 1 if sc.dtype == np.uint16 else 0
+    sc = np.ascontiguousarray(sc, dtype=np.uint16 if scores_bf16 else np.float32)
+    T, D = x.shape
+    E, _, F, _ = w13.shape
+    K = ids.shape[1]
+    out = np.zeros((T, D), np.float32)
+    rc = _library(lib).oracle_routed_experts_rmsnorm(
+        _ptr(x), _ptr(ids), _ptr(sc), scores_bf16, _ptr(w13), _ptr(w2), _ptr(out),
+        T, D, F, E, K, float(eps), int(nthreads or os.cpu_count() or 1),
+    )
+    if rc != 0:
+        raise RuntimeError("oracle_routed_experts_rmsnorm failed")
     return out
 
 

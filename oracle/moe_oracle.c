@@ -127,6 +127,8 @@ typedef struct {
     int64_t t_begin, t_end;
     int32_t D, F, E, K;
     int round_h;
+    int rmsnorm;       /* 1: route-wise RMSNorm of each expert output before the score */
+    float rms_eps;
     int failed;
 } oracle_job;
 
@@ -142,11 +144,13 @@ static void *oracle_tokens(void *arg) {
     float *xt = (float *)malloc(sizeof(float) * (size_t)D);
     float *acc = (float *)malloc(sizeof(float) * (size_t)D);
     float *h = (float *)malloc(sizeof(float) * (size_t)F);
-    if (!xt || !acc || !h) {
+    float *xt_y = (float *)malloc(sizeof(float) * (size_t)D);
+    if (!xt || !acc || !h || !xt_y) {
         job->failed = 1;
         free(xt);
         free(acc);
         free(h);
+        free(xt_y);
         return NULL;
     }
     for (int64_t t = job->t_begin; t < job->t_end; ++t) {
@@ -171,10 +175,23 @@ static void *oracle_tokens(void *arg) {
                 if (job->round_h) h[f] = round_to_bf16(h[f]);
             }
             /* down projection, weighted by the pair's score */
-            for (int32_t j = 0; j < D; ++j) {
-                float y = 0.0f;
-                for (int32_t f = 0; f < F; ++f) y += bf16_to_f32(w2e[(size_t)j * F + f]) * h[f];
-                acc[j] += s * y;
+            if (!job->rmsnorm) {
+                for (int32_t j = 0; j < D; ++j) {
+                    float y = 0.0f;
+                    for (int32_t f = 0; f < F; ++f) y += bf16_to_f32(w2e[(size_t)j * F + f]) * h[f];
+                    acc[j] += s * y;
+                }
+            } else {
+                /* route-wise RMSNorm: y / sqrt(mean(y^2) + eps), then the score */
+                float ss = 0.0f;
+                for (int32_t j = 0; j < D; ++j) {
+                    float y = 0.0f;
+                    for (int32_t f = 0; f < F; ++f) y += bf16_to_f32(w2e[(size_t)j * F + f]) * h[f];
+                    xt_y[j] = y;
+                    ss += y * y;
+                }
+                const float rstd = 1.0f / sqrtf(ss / (float)D + job->rms_eps);
+                for (int32_t j = 0; j < D; ++j) acc[j] += s * (xt_y[j] * rstd);
             }
         }
         for (int32_t j = 0; j < D; ++j) job->out[t * D + j] = acc[j];
@@ -182,7 +199,27 @@ static void *oracle_tokens(void *arg) {
     free(xt);
     free(acc);
     free(h);
+    free(xt_y);
     return NULL;
+}
+
+static int oracle_forward(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
+                          const uint16_t *w13, const uint16_t *w2, float *out, int64_t T, int32_t D,
+                          int32_t F, int32_t E, int32_t K, int round_h, int rmsnorm, float rms_eps,
+                          int nthreads);
+
+/*
+ * The forward with Dist-MoE's typed post-expert processing (Dist-MoE 0.1.0, "Use advanced
+ * features / Post-expert processing": route-wise RMSNorm, router-score weighting and top-k
+ * reduction in one step):
+ *     out[t] = sum_k score[t,k] * y / sqrt(mean_d(y^2) + eps),   y = W2[e] (SiLU(Wg[e] x_t) * Wu[e] x_t)
+ * Reading: the normalisation has no gain vector (the page names only eps and dtypes); the norm
+ * is taken in fp32 (its norm_output_dtype) and the sum in fp32.
+ */
+int oracle_routed_experts_rmsnorm(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
+                                  const uint16_t *w13, const uint16_t *w2, float *out, int64_t T, int32_t D,
+                                  int32_t F, int32_t E, int32_t K, float eps, int nthreads) {
+    return oracle_forward(x, ids, scores, scores_bf16, w13, w2, out, T, D, F, E, K, 0, 1, eps, nthreads);
 }
 
 /*
@@ -192,9 +229,10 @@ static void *oracle_tokens(void *arg) {
  * threads (each token is computed by one thread, in the same order, whatever nthreads is).
  * Returns 0, or -1 on a bad argument or an allocation failure.
  */
-int oracle_routed_experts(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
+static int oracle_forward(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
                           const uint16_t *w13, const uint16_t *w2, float *out, int64_t T, int32_t D,
-                          int32_t F, int32_t E, int32_t K, int round_h, int nthreads) {
+                          int32_t F, int32_t E, int32_t K, int round_h, int rmsnorm, float rms_eps,
+                          int nthreads) {
     if (T < 0 || D <= 0 || F <= 0 || E <= 0 || K <= 0) return -1;
     if (T == 0) return 0;
     if (nthreads < 1) nthreads = 1;
@@ -223,6 +261,8 @@ int oracle_routed_experts(const uint16_t *x, const int32_t *ids, const void *sco
         j->E = E;
         j->K = K;
         j->round_h = round_h;
+        j->rmsnorm = rmsnorm;
+        j->rms_eps = rms_eps;
     }
     unsigned char *running = (unsigned char *)calloc((size_t)nthreads, 1);
     if (!running) {
@@ -243,6 +283,12 @@ int oracle_routed_experts(const uint16_t *x, const int32_t *ids, const void *sco
     free(jobs);
     free(tids);
     return rc;
+}
+
+int oracle_routed_experts(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
+                          const uint16_t *w13, const uint16_t *w2, float *out, int64_t T, int32_t D,
+                          int32_t F, int32_t E, int32_t K, int round_h, int nthreads) {
+    return oracle_forward(x, ids, scores, scores_bf16, w13, w2, out, T, D, F, E, K, round_h, 0, 0.0f, nthreads);
 }
 
 /* ------------------------------------------------------------------------------------------ */

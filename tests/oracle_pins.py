@@ -287,3 +287,58 @@ OUTPUT_PINS = [
     check_thread_count_invariance,
 ]
 ALL_PINS = ROUTING_PINS + OUTPUT_PINS
+
+
+# -------------------------------------------------------------------- RMSNorm post-processing
+
+def run_rms(p, eps, lib=None):
+    return oracle.routed_experts_rmsnorm(p["x"], p["ids"], p["scores"], p["w13"], p["w2"], eps, lib=lib)
+
+
+def check_rmsnorm_vs_torch(lib=None):
+    # every expert on every token in float64, torch's own rms_norm per (token, expert), contracted
+    # with the dense score matrix
+    for c in (dict(T=9, D=32, F=48, E=5, K=3, seed=31), dict(T=11, D=64, F=32, E=4, K=2, seed=32, dup=True,
+                                                                 invalid_frac=0.2, zero_frac=0.2)):
+        p = small_problem(**c)
+        x = torch.from_numpy(bits_to_f64(p["x"]))
+        w13 = torch.from_numpy(bits_to_f64(p["w13"]))
+        w2 = torch.from_numpy(bits_to_f64(p["w2"]))
+        h = Fnn.silu(torch.einsum("efd,td->tef", w13[:, 0], x)) * torch.einsum("efd,td->tef", w13[:, 1], x)
+        y = torch.einsum("edf,tef->ted", w2, h)
+        z = Fnn.rms_norm(y, (c["D"],), eps=1e-6)
+        E = c["E"]
+        S = np.zeros((c["T"], E))
+        for t in range(c["T"]):
+            for k in range(c["K"]):
+                e = int(p["ids"][t, k])
+                if 0 <= e < E:
+                    S[t, e] += float(p["scores"][t, k])
+        ref = torch.einsum("te,ted->td", torch.from_numpy(S), z).numpy()
+        assert max_rel_err(run_rms(p, 1e-6, lib), ref) <= ORACLE_FP32_TOL
+
+
+def check_rmsnorm_scale_invariance(lib=None):
+    # with eps = 0 the normalised output does not depend on the scale of W2: x4 is exact in bf16
+    # and in every fp32 step, so the outputs are bit-identical
+    p = small_problem(T=10, D=32, F=32, E=3, K=2, seed=33)
+    a = run_rms(p, 0.0, lib)
+    w2 = torch.from_numpy(bits_to_f64(p["w2"])).float() * 4.0
+    b = run_rms(dict(p, w2=bf16_bits(w2.to(torch.bfloat16))), 0.0, lib)
+    assert np.array_equal(a, b)
+
+
+def check_rmsnorm_scalar_sign(lib=None):
+    # D = 1 and eps = 0: RMSNorm of a scalar is its sign, so out = sum_k s * sign(y_k)
+    p = small_problem(T=6, D=1, F=8, E=3, K=2, seed=34)
+    y = oracle.routed_experts(p["x"], p["ids"][:, :1].copy(), np.ones((6, 1), np.float32), p["w13"], p["w2"],
+                              lib=lib)[:, 0]
+    y2 = oracle.routed_experts(p["x"], p["ids"][:, 1:].copy(), np.ones((6, 1), np.float32), p["w13"], p["w2"],
+                               lib=lib)[:, 0]
+    ref = p["scores"][:, 0] * np.sign(y) + p["scores"][:, 1] * np.sign(y2)
+    got = run_rms(p, 0.0, lib)[:, 0]
+    assert np.allclose(got, ref, rtol=1e-6, atol=1e-7)
+
+
+OUTPUT_PINS += [check_rmsnorm_vs_torch, check_rmsnorm_scale_invariance, check_rmsnorm_scalar_sign]
+ALL_PINS = ROUTING_PINS + OUTPUT_PINS

@@ -98,7 +98,8 @@ def test_workspace_layout(lib, dims):
     lay = binding.moe_workspace_layout(*dims)
     R = T * K
     sizes = {"status": 4, "counts": 4 * E, "offsets": 4 * (E + 1), "tiles1": 4 * (E + 1), "tiles2": 4 * (E + 1),
-             "perm": 4 * R, "inv": 4 * R, "xp": 2 * R * D, "h": 2 * R * F}
+             "perm": 4 * R, "inv": 4 * R, "xp": 2 * R * D, "h": 2 * R * F,
+             "rms": 4 * R * ((D + 255) // 256)}
     names = list(binding.WS_REGIONS)
     for i, name in enumerate(names[:-1]):
         assert lay[name] % 256 == 0
@@ -108,3 +109,36 @@ def test_workspace_layout(lib, dims):
     assert lay["status"] == 0
     assert lay["total"] == binding.moe_workspace_bytes(*dims)
     assert binding.moe_routing_workspace_bytes(T, E, K) < lay["total"]
+
+
+def bwd(lib, **kw):
+    a = dict(x=FAKE, ids=FAKE, scores=FAKE, sd=0, w13=FAKE, w2=FAKE, dout=FAKE, dx=FAKE, dsc=FAKE, dw13=FAKE,
+             dw2=FAKE, T=16, D=256, F=256, E=8, K=2, ws=FAKE, wsb=1 << 40)
+    a.update(kw)
+    v = ctypes.c_void_p
+    return lib.moe_routed_experts_bwd(v(a["x"]), v(a["ids"]), v(a["scores"]), a["sd"], v(a["w13"]), v(a["w2"]),
+                                      v(a["dout"]), v(a["dx"]), v(a["dsc"]), v(a["dw13"]), v(a["dw2"]), a["T"],
+                                      a["D"], a["F"], a["E"], a["K"], v(a["ws"]), a["wsb"], None)
+
+
+def test_bwd_host_validation_needs_no_gpu(lib):
+    assert bwd(lib, T=-1) == INVALID
+    assert bwd(lib, sd=3) == INVALID
+    assert bwd(lib, dw2=0) == INVALID
+    assert bwd(lib, dout=0) == INVALID
+    assert bwd(lib, ws=0) == INVALID
+    assert bwd(lib, D=96) == SHAPE
+    assert bwd(lib, E=5000) == SHAPE
+    assert bwd(lib, dx=FAKE + 8) == MISALIGNED
+    assert bwd(lib, dw13=FAKE + 2) == MISALIGNED
+    assert bwd(lib, dsc=FAKE + 2) == MISALIGNED
+    need = binding.moe_bwd_workspace_bytes(16, 256, 256, 8, 2)
+    assert need > binding.moe_workspace_bytes(16, 256, 256, 8, 2)
+    assert bwd(lib, wsb=need - 1) == WS_SMALL
+    assert binding.moe_bwd_workspace_bytes(0, 256, 256, 8, 2) == 0
+
+
+def test_binding_region_list_matches_header():
+    text = open(HEADER).read()
+    n = int(re.search(r"MOE_WS_REGIONS\s*=\s*(\d+)", text).group(1))
+    assert len(binding.WS_REGIONS) == n

@@ -139,3 +139,24 @@ def test_bwd_medium_workload_subsets():
     ref, remap = compact(tokens)
     assert max_rel_err(got["dw13"][e].float().cpu().numpy(), ref["dw13"][remap[e]]) <= TOL
     assert max_rel_err(got["dw2"][e].float().cpu().numpy(), ref["dw2"][remap[e]]) <= TOL
+
+
+def test_bwd_bf16_scores():
+    d = problem(90, 256, 128, 4, 2)
+    d["topk_scores"] = d["topk_scores"].to(torch.bfloat16)
+    got, _ = run_bwd(d)
+    check_all(got, oracle_bwd(d))
+
+
+def test_bwd_no_tokens_gives_zero_weight_gradients():
+    E, D, F = 3, 128, 64
+    w13, w2 = W.make_weights(E, D, F, 0, "cuda")
+    dw13 = torch.full_like(w13, 7.0)
+    dw2 = torch.full_like(w2, 7.0)
+    x = torch.empty((0, D), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    sc = torch.empty((0, 2), dtype=torch.float32, device="cuda")
+    ws = binding.alloc_workspace(256, "cuda")
+    binding.moe_routed_experts_bwd(x, ids, sc, w13, w2, x, torch.empty_like(x), sc.clone(), dw13, dw2, ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dw13) == 0 and torch.count_nonzero(dw2) == 0

@@ -169,3 +169,33 @@ def test_medium_workload_token_subset():
     tokens = np.random.default_rng(0).choice(d["x"].shape[0], 24, replace=False)
     ref, tok = oracle_tokens(d, tokens)
     assert max_rel_err(out[torch.from_numpy(tok).cuda()].float().cpu().numpy(), ref) <= OUT_TOL
+
+
+@pytest.mark.parametrize("name", ["ragged_multi_tile", "partial_down_tile", "skew"])
+def test_fwd_rmsnorm_matches_oracle(name):
+    import oracle
+    from common import bf16_bits
+    from gpu_common import scores_host
+
+    T, D, F, E, K, routing = CASES[name]
+    d = problem(T, D, F, E, K, routing)
+    out = torch.empty_like(d["x"])
+    ws = binding.alloc_workspace(binding.moe_workspace_bytes(T, D, F, E, K), "cuda")
+    binding.moe_routed_experts_fwd_rmsnorm(d["x"], d["topk_ids"], d["topk_scores"], d["w13"], d["w2"], out, ws,
+                                           eps=1e-6)
+    ref = oracle.routed_experts_rmsnorm(bf16_bits(d["x"]), d["topk_ids"].cpu().numpy(), scores_host(d["topk_scores"]),
+                                        bf16_bits(d["w13"]), bf16_bits(d["w2"]), 1e-6)
+    assert max_rel_err(out.float().cpu().numpy(), ref) <= OUT_TOL
+    assert binding.moe_get_status(ws) == 0
+
+
+def test_fwd_rmsnorm_ignores_w2_scale():
+    # RMSNorm makes each expert output scale-free: scaling W2 by 4 leaves the result (nearly) unchanged
+    d = problem(120, 256, 128, 4, 2)
+    ws = binding.alloc_workspace(binding.moe_workspace_bytes(120, 256, 128, 4, 2), "cuda")
+    a = torch.empty_like(d["x"])
+    b = torch.empty_like(d["x"])
+    binding.moe_routed_experts_fwd_rmsnorm(d["x"], d["topk_ids"], d["topk_scores"], d["w13"], d["w2"], a, ws, eps=0.0)
+    w2x4 = (d["w2"].float() * 4).to(torch.bfloat16)
+    binding.moe_routed_experts_fwd_rmsnorm(d["x"], d["topk_ids"], d["topk_scores"], d["w13"], w2x4, b, ws, eps=0.0)
+    assert torch.equal(a, b)

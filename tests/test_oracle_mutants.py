@@ -33,6 +33,11 @@ MUTANTS = {
     "invalid_ids_kept": [("int32_t key = (e >= 0 && e < E) ? e : E;", "int32_t key = (e >= 0 && e < E) ? e : 0;")],
     "inv_identity": [("inv[i] = (int32_t)r;", "inv[i] = (int32_t)i;")],
     "round_h_truncates": [("u += 0x7fffu + ((u >> 16) & 1u);", "u += 0u;")],
+    # route-wise RMSNorm post-processing
+    "rms_sum_not_mean": [("const float rstd = 1.0f / sqrtf(ss / (float)D + job->rms_eps);",
+                          "const float rstd = 1.0f / sqrtf(ss + job->rms_eps);")],
+    "rms_score_dropped": [("for (int32_t j = 0; j < D; ++j) acc[j] += s * (xt_y[j] * rstd);",
+                           "for (int32_t j = 0; j < D; ++j) acc[j] += (xt_y[j] * rstd);")],
     # backward
     "bwd_silu_grad_sign": [("return sig * (1.0f + g * (1.0f - sig));", "return sig * (1.0f - g * (1.0f - sig));")],
     "bwd_dh_without_score": [("const float dh = s * w2t[f];", "const float dh = w2t[f];")],

@@ -69,6 +69,13 @@ def load_library(path: str) -> ctypes.CDLL:
         ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
     ]
     lib.oracle_routed_experts_bwd.restype = ctypes.c_int
+    lib.oracle_mx_quantize_rows.argtypes = [p, ctypes.c_int64, ctypes.c_int32, p, p]
+    lib.oracle_mx_quantize_rows.restype = ctypes.c_int
+    lib.oracle_routed_experts_mxfp8.argtypes = [
+        p, p, p, ctypes.c_int, p, p, p, p, p,
+        ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+    ]
+    lib.oracle_routed_experts_mxfp8.restype = ctypes.c_int
     return lib
 
 
@@ -198,4 +205,71 @@ def routed_experts_bwd(x_bits, topk_ids, topk_scores, w13_bits, w2_bits, dout, n
     )
     if rc != 0:
         raise RuntimeError("oracle_routed_experts_bwd failed")
+    return out
+
+
+def mx_quantize_rows(bits, lib=None):
+    """MX (E4M3 elements, UE8M0 scales, blocks of 32 along the last axis) quantization of bf16 bits.
+
+    ``bits`` is a uint16 array ``[..., cols]`` with ``cols % 32 == 0``. Returns ``(codes, scales)``:
+    uint8 E4M3 codes of the same shape and uint8 UE8M0 scale codes ``[..., cols // 32]``.
+    """
+    a = np.ascontiguousarray(bits, dtype=np.uint16)
+    cols = a.shape[-1]
+    rows = a.size // cols if cols else 0
+    codes = np.zeros(a.shape, np.uint8)
+    scales = np.zeros(a.shape[:-1] + (cols // 32,), np.uint8)
+    if _library(lib).oracle_mx_quantize_rows(_ptr(a), rows, cols, _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError("oracle_mx_quantize_rows rejected its arguments")
+    return codes, scales
+
+
+def e4m3_values(codes) -> np.ndarray:
+    """float64 values of E4M3 codes (the format's definition; 0x7F / 0xFF, NaN, never occur)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    ex = (c >> 3) & 15
+    man = c & 7
+    mag = np.where(ex == 0, np.ldexp(man.astype(np.float64), -9),
+                   np.ldexp((8 + man).astype(np.float64), ex - 10))
+    return sign * mag
+
+
+def mx_dequantize(codes, scales) -> np.ndarray:
+    """float64 values of an MX-quantized array: value(code) * 2^(scale - 127) per block of 32."""
+    v = e4m3_values(codes)
+    e = np.repeat(np.asarray(scales, dtype=np.int64) - 127, 32, axis=-1)
+    return np.ldexp(v, e)
+
+
+def routed_experts_mxfp8(x_bits, topk_ids, topk_scores, w13_mx, w2_mx, nthreads: int | None = None,
+                         lib=None) -> np.ndarray:
+    """out[T,D] (fp32) of the MXFP8 forward.
+
+    ``x_bits`` [T,D] bf16 bits (quantized here, per token row); ``w13_mx`` = (codes [E,2,F,D],
+    scales [E,2,F,D/32]) and ``w2_mx`` = (codes [E,D,F], scales [E,D,F/32]) as returned by
+    :func:`mx_quantize_rows` on the bf16 weights. ids and scores as for :func:`routed_experts`.
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    w13q, w13s = (np.ascontiguousarray(a, dtype=np.uint8) for a in w13_mx)
+    w2q, w2s = (np.ascontiguousarray(a, dtype=np.uint8) for a in w2_mx)
+    sc = np.asarray(topk_scores)
+    scores_bf16 = 1 if sc.dtype == np.uint16 else 0
+    sc = np.ascontiguousarray(sc, dtype=np.uint16 if scores_bf16 else np.float32)
+    T, D = x.shape
+    E, two, F, D2 = w13q.shape
+    K = ids.shape[1]
+    if (two != 2 or D2 != D or w13s.shape != (E, 2, F, D // 32) or w2q.shape != (E, D, F)
+            or w2s.shape != (E, D, F // 32) or ids.shape[0] != T or sc.shape != ids.shape):
+        raise ValueError("inconsistent shapes")
+    out = np.zeros((T, D), np.float32)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _library(lib).oracle_routed_experts_mxfp8(
+        _ptr(x), _ptr(ids), _ptr(sc), scores_bf16, _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s), _ptr(out),
+        T, D, F, E, K, int(nthreads),
+    )
+    if rc != 0:
+        raise RuntimeError("oracle_routed_experts_mxfp8 failed")
     return out

@@ -23,7 +23,10 @@
  * is fp32, summed in ascending index order, as the pages' BF16 path accumulates in FP32. Built
  * with -ffp-contract=off so no multiply-add is fused and x86 and Arm hosts give the same bits.
  *
- * The backward pass (oracle_routed_experts_bwd, at the end of this file) is the same definition
+ * The MXFP8 forward (oracle_routed_experts_mxfp8, after the backward) is the same definition with
+ * block-scaled E4M3 operands; its own header states the format it reads.
+ *
+ * The backward pass (oracle_routed_experts_bwd) is the same definition
  * differentiated by hand; the pages name its parts (Dist-MoE 0.1.0, "Understand the execution
  * model": DGRAD computes input gradients and WGRAD weight gradients; TeraMoE README, usage
  * example: output.backward(...)).
@@ -129,6 +132,8 @@ typedef struct {
     int round_h;
     int rmsnorm;       /* 1: route-wise RMSNorm of each expert output before the score */
     float rms_eps;
+    /* MXFP8 forward only: prepared weights as E4M3 codes and UE8M0 block-scale codes */
+    const uint8_t *w13q, *w13s, *w2q, *w2s;
     int failed;
 } oracle_job;
 
@@ -500,6 +505,227 @@ int oracle_routed_experts_bwd(const uint16_t *x, const int32_t *ids, const void 
     }
 done:
     free(fws);
+    free(jobs);
+    free(tids);
+    free(running);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* MXFP8 forward.                                                                              */
+/*                                                                                             */
+/* Dist-MoE 0.1.0, "Choose a precision and pipeline / MXFP8": the MXFP8 E4M3 format; activations */
+/* are quantized after routing and the weights are prepared once ("Use advanced features /      */
+/* Prepared block-scaled weights"); tensor-core products accumulate in FP32. The page names the  */
+/* format but not its encoding. The reading here is the OCP Microscaling (MX) format, v1.0:     */
+/*   - a block is 32 consecutive elements along the contraction axis of a GEMM operand (D for x  */
+/*     and w13, F for the SwiGLU output h and w2);                                               */
+/*   - the block shares one power-of-two scale X = 2^e, stored as the UE8M0 code e + 127, with  */
+/*     e = floor(log2(max|v|)) - 8 (8 = the exponent of E4M3's largest normal, 448 = 1.75*2^8), */
+/*     clamped to [-127, 127]; an all-zero block gets e = -127;                                 */
+/*   - each element is v / X rounded to the nearest E4M3 value, ties to even, magnitudes beyond  */
+/*     448 saturating to 448, the sign kept (so a negative value that rounds to zero is -0);     */
+/*   - the block's value is code * X.                                                            */
+/* x is quantized per token row (a routed row is a copy of it), h per pair after SwiGLU in fp32. */
+/* Every product of dequantized operands and every sum is fp32, in ascending index order.        */
+
+/* Value of an E4M3 code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 */
+/* holds the subnormals m * 2^-9; 0x7F and 0xFF are NaN and never produced here).               */
+static double e4m3_value(uint8_t code) {
+    const int sign = code >> 7, ex = (code >> 3) & 15, man = code & 7;
+    const double mag = ex == 0 ? ldexp((double)man, -9) : ldexp((double)(8 + man), ex - 10);
+    return sign ? -mag : mag;
+}
+
+/* The E4M3 code nearest to v (ties to even, |v| beyond 448 gives 448, the sign of v kept). The  */
+/* representable magnitudes in [2^k, 2^(k+1)) are spaced 2^(k-3) for k >= -6; below 2^-6 they   */
+/* are the subnormals, spaced 2^-9.                                                              */
+static uint8_t e4m3_code(double v) {
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs(v);
+    int ex = 0;
+    if (a > 0) (void)frexp(a, &ex); /* a = f 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1 */
+    const int k = (a > 0 && ex - 1 > -6) ? ex - 1 : -6;
+    double r = ldexp(nearbyint(ldexp(a, 3 - k)), k - 3); /* default rounding mode: ties to even */
+    if (r > 448.0) r = 448.0;
+    if (r == 0) return sign;
+    int rex = 0;
+    (void)frexp(r, &rex);
+    const int rk = rex - 1;
+    if (rk < -6) return (uint8_t)(sign | (uint8_t)ldexp(r, 9)); /* subnormal: m 2^-9 */
+    return (uint8_t)(sign | (uint8_t)((rk + 7) << 3) | (uint8_t)((int)ldexp(r, 3 - rk) - 8));
+}
+
+/* Scale exponent of a block with largest magnitude amax. */
+static int mx_exponent(double amax) {
+    if (!(amax > 0)) return -127;
+    int ex = 0;
+    (void)frexp(amax, &ex);
+    int e = (ex - 1) - 8;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* Quantize n = 32 values: codes[0..31] and the block's UE8M0 scale code. */
+static void mx_quantize_block(const float *v, uint8_t *codes, uint8_t *scale_code) {
+    double amax = 0;
+    for (int i = 0; i < 32; ++i)
+        if (fabs((double)v[i]) > amax) amax = fabs((double)v[i]);
+    const int e = mx_exponent(amax);
+    for (int i = 0; i < 32; ++i) codes[i] = e4m3_code(ldexp((double)v[i], -e));
+    *scale_code = (uint8_t)(e + 127);
+}
+
+/*
+ * MX quantization of a bf16 matrix [rows, cols] along its rows (cols % 32 == 0): E4M3 codes
+ * [rows, cols] and UE8M0 scale codes [rows, cols / 32], both row-major. This is how the MXFP8
+ * weights are prepared: w13 [E, 2F, D] as E*2F rows of D, w2 [E, D, F] as E*D rows of F.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_mx_quantize_rows(const uint16_t *in, int64_t rows, int32_t cols, uint8_t *codes, uint8_t *scales) {
+    if (rows < 0 || cols <= 0 || cols % 32 != 0) return -1;
+    float blk[32];
+    for (int64_t r = 0; r < rows; ++r)
+        for (int32_t b = 0; b < cols / 32; ++b) {
+            for (int i = 0; i < 32; ++i) blk[i] = bf16_to_f32(in[r * cols + b * 32 + i]);
+            mx_quantize_block(blk, codes + r * cols + b * 32, scales + r * (cols / 32) + b);
+        }
+    return 0;
+}
+
+/* Dequantized row: out[i] = value(codes[i]) * 2^(scales[i / 32] - 127), exact in fp32. `value`
+ * is a table of e4m3_value over all 256 codes (each worker thread fills its own). */
+static void mx_dequantize_row(const double *value, const uint8_t *codes, const uint8_t *scales, int32_t cols,
+                              float *out) {
+    for (int32_t b = 0; b < cols / 32; ++b) {
+        const int e = (int)scales[b] - 127;
+        for (int i = 0; i < 32; ++i) out[b * 32 + i] = (float)ldexp(value[codes[b * 32 + i]], e);
+    }
+}
+
+static void *oracle_tokens_mxfp8(void *arg) {
+    oracle_job *job = (oracle_job *)arg;
+    const int32_t D = job->D, F = job->F, E = job->E, K = job->K;
+    float *xt = (float *)malloc(sizeof(float) * (size_t)D);
+    float *xd = (float *)malloc(sizeof(float) * (size_t)D);
+    float *acc = (float *)malloc(sizeof(float) * (size_t)D);
+    float *h = (float *)malloc(sizeof(float) * (size_t)F);
+    float *hd = (float *)malloc(sizeof(float) * (size_t)F);
+    float *wg = (float *)malloc(sizeof(float) * (size_t)D);
+    float *wu = (float *)malloc(sizeof(float) * (size_t)D);
+    float *w2r = (float *)malloc(sizeof(float) * (size_t)F);
+    uint8_t *q = (uint8_t *)malloc((size_t)(D > F ? D : F));
+    uint8_t *qs = (uint8_t *)malloc((size_t)(D > F ? D : F) / 32);
+    double value[256];
+    if (!xt || !xd || !acc || !h || !hd || !wg || !wu || !w2r || !q || !qs) {
+        job->failed = 1;
+        goto out;
+    }
+    for (int c = 0; c < 256; ++c) value[c] = e4m3_value((uint8_t)c);
+    for (int64_t t = job->t_begin; t < job->t_end; ++t) {
+        /* the token row, quantized and dequantized */
+        for (int32_t b = 0; b < D / 32; ++b) {
+            for (int i = 0; i < 32; ++i) xt[b * 32 + i] = bf16_to_f32(job->x[t * D + b * 32 + i]);
+            mx_quantize_block(xt + b * 32, q + b * 32, qs + b);
+        }
+        mx_dequantize_row(value, q, qs, D, xd);
+        for (int32_t j = 0; j < D; ++j) acc[j] = 0.0f;
+        for (int32_t k = 0; k < K; ++k) {
+            const int32_t e = job->ids[t * K + k];
+            if (e < 0 || e >= E) continue;
+            const float s = pair_score(job, t * K + k);
+            /* gate/up projection and SwiGLU, from dequantized operands */
+            for (int32_t f = 0; f < F; ++f) {
+                const size_t grow = ((size_t)e * 2 + 0) * (size_t)F + (size_t)f; /* row of [E*2F, D] */
+                const size_t urow = ((size_t)e * 2 + 1) * (size_t)F + (size_t)f;
+                mx_dequantize_row(value, job->w13q + grow * (size_t)D, job->w13s + grow * (size_t)(D / 32), D, wg);
+                mx_dequantize_row(value, job->w13q + urow * (size_t)D, job->w13s + urow * (size_t)(D / 32), D, wu);
+                float g = 0.0f, u = 0.0f;
+                for (int32_t d = 0; d < D; ++d) {
+                    g += wg[d] * xd[d];
+                    u += wu[d] * xd[d];
+                }
+                h[f] = g / (1.0f + expf(-g)) * u;
+            }
+            /* h quantized after SwiGLU, then the down projection weighted by the score */
+            for (int32_t b = 0; b < F / 32; ++b) mx_quantize_block(h + b * 32, q + b * 32, qs + b);
+            mx_dequantize_row(value, q, qs, F, hd);
+            for (int32_t j = 0; j < D; ++j) {
+                const size_t row = (size_t)e * (size_t)D + (size_t)j; /* row of [E*D, F] */
+                mx_dequantize_row(value, job->w2q + row * (size_t)F, job->w2s + row * (size_t)(F / 32), F, w2r);
+                float y = 0.0f;
+                for (int32_t f = 0; f < F; ++f) y += w2r[f] * hd[f];
+                acc[j] += s * y;
+            }
+        }
+        for (int32_t j = 0; j < D; ++j) job->out[t * D + j] = acc[j];
+    }
+out:
+    free(xt);
+    free(xd);
+    free(acc);
+    free(h);
+    free(hd);
+    free(wg);
+    free(wu);
+    free(w2r);
+    free(q);
+    free(qs);
+    return NULL;
+}
+
+/*
+ * out[T,D] (fp32) of the MXFP8 forward. x [T,D] bf16 bits; ids, scores as for
+ * oracle_routed_experts; the weights prepared by oracle_mx_quantize_rows: w13q [E,2F,D] codes with
+ * w13s [E,2F,D/32] scale codes, w2q [E,D,F] codes with w2s [E,D,F/32]. D and F must be multiples
+ * of 32. Tokens are split across nthreads threads as in oracle_routed_experts.
+ * Returns 0, or -1 on a bad argument or an allocation failure.
+ */
+int oracle_routed_experts_mxfp8(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
+                                const uint8_t *w13q, const uint8_t *w13s, const uint8_t *w2q,
+                                const uint8_t *w2s, float *out, int64_t T, int32_t D, int32_t F, int32_t E,
+                                int32_t K, int nthreads) {
+    if (T < 0 || D <= 0 || F <= 0 || E <= 0 || K <= 0 || D % 32 != 0 || F % 32 != 0) return -1;
+    if (T == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > T) nthreads = (int)T;
+    oracle_job *jobs = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    unsigned char *running = (unsigned char *)calloc((size_t)nthreads, 1);
+    int rc = 0;
+    if (!jobs || !tids || !running) {
+        rc = -1;
+        goto done;
+    }
+    for (int i = 0; i < nthreads; ++i) {
+        oracle_job *j = &jobs[i];
+        j->x = x;
+        j->ids = ids;
+        j->scores = scores;
+        j->scores_bf16 = scores_bf16;
+        j->w13q = w13q;
+        j->w13s = w13s;
+        j->w2q = w2q;
+        j->w2s = w2s;
+        j->out = out;
+        j->t_begin = T * i / nthreads;
+        j->t_end = T * (i + 1) / nthreads;
+        j->D = D;
+        j->F = F;
+        j->E = E;
+        j->K = K;
+    }
+    for (int i = 1; i < nthreads; ++i)
+        running[i] = (pthread_create(&tids[i], NULL, oracle_tokens_mxfp8, &jobs[i]) == 0);
+    oracle_tokens_mxfp8(&jobs[0]);
+    for (int i = 1; i < nthreads; ++i)
+        if (running[i]) pthread_join(tids[i], NULL);
+    for (int i = 1; i < nthreads; ++i)
+        if (!running[i]) oracle_tokens_mxfp8(&jobs[i]);
+    for (int i = 0; i < nthreads; ++i)
+        if (jobs[i].failed) rc = -1;
+done:
     free(jobs);
     free(tids);
     free(running);

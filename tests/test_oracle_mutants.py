@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 import oracle_bwd_pins
+import oracle_mx_pins
 import oracle_pins
 
 MUTANTS = {
@@ -46,6 +47,22 @@ MUTANTS = {
     "bwd_dscore_scaled": [("ds += w2t[f] * h[f];", "ds += w2t[f] * h[f] * s;")],
     "bwd_du_from_gate": [("du[f] = dh * a[f];", "du[f] = dh * g[f];")],
     "bwd_dwu_from_dg": [("dwu[(size_t)f * D + d] += du[f] * xt[d];", "dwu[(size_t)f * D + d] += dg[f] * xt[d];")],
+    # MXFP8: the MX format and the block-scaled forward
+    "mx_scale_off_by_one": [("int e = (ex - 1) - 8;", "int e = ex - 8;")],
+    "mx_emax_of_e5m2": [("int e = (ex - 1) - 8;", "int e = (ex - 1) - 15;")],
+    "mx_no_saturation": [("if (r > 448.0) r = 448.0;", "")],
+    "mx_ties_away_from_zero": [("nearbyint(ldexp(a, 3 - k))", "round(ldexp(a, 3 - k))")],
+    "mx_amax_over_half_block": [("for (int i = 0; i < 32; ++i)\n        if (fabs((double)v[i]) > amax)",
+                                 "for (int i = 0; i < 16; ++i)\n        if (fabs((double)v[i]) > amax)")],
+    "mx_zero_loses_sign": [("if (r == 0) return sign;", "if (r == 0) return 0;")],
+    "mx_no_subnormals": [("const int k = (a > 0 && ex - 1 > -6) ? ex - 1 : -6;",
+                          "const int k = (a > 0) ? ex - 1 : -6;")],
+    "mx_e4m3_bias": [("ldexp((double)(8 + man), ex - 10)", "ldexp((double)(8 + man), ex - 11)")],
+    "mx_scale_sign": [("ldexp(value[codes[b * 32 + i]], e)", "ldexp(value[codes[b * 32 + i]], -e)")],
+    "mx_h_not_quantized": [("mx_dequantize_row(value, q, qs, F, hd);", "memcpy(hd, h, sizeof(float) * (size_t)F);")],
+    "mx_x_not_quantized": [("g += wg[d] * xd[d];\n                    u += wu[d] * xd[d];",
+                            "g += wg[d] * xt[d];\n                    u += wu[d] * xt[d];")],
+    "mx_gate_uses_up_scales": [("job->w13s + grow * (size_t)(D / 32)", "job->w13s + urow * (size_t)(D / 32)")],
 }
 
 
@@ -62,7 +79,7 @@ def test_pins_reject_mutant(name, tmp_path):
     oracle.compile_oracle(str(path), lib_path)
     lib = oracle.load_library(lib_path)
     failed = []
-    for check in oracle_pins.ALL_PINS + oracle_bwd_pins.BWD_PINS:
+    for check in oracle_pins.ALL_PINS + oracle_bwd_pins.BWD_PINS + oracle_mx_pins.MX_PINS:
         try:
             check(lib=lib)
         except AssertionError:

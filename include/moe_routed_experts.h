@@ -234,6 +234,102 @@ moe_status_t moe_routed_experts_bwd(const void *x, const int32_t *topk_ids, cons
                                     int32_t F, int32_t E, int32_t K, void *workspace, size_t workspace_bytes,
                                     moe_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------ */
+/* MXFP8 forward (Dist-MoE 0.1.0, "Choose a precision and pipeline / MXFP8": MXFP8 E4M3, the    */
+/* activations quantized after routing, the weights prepared once and reused -- "Use advanced   */
+/* features / Prepared block-scaled weights" -- and FP32 accumulation).                        */
+/*                                                                                              */
+/* The format, read as the OCP Microscaling (MX) v1.0 format: a block is 32 consecutive elements */
+/* along a GEMM's contraction axis (D for x and w13, F for the SwiGLU output h and for w2); it  */
+/* shares the scale 2^e, e = floor(log2 max|v|) - 8 clamped to [-127, 127] (an all-zero block:  */
+/* -127), stored as the UE8M0 byte e + 127; each element is the E4M3 value nearest v * 2^-e     */
+/* (ties to even, saturating at 448, sign kept). x is quantized per token row, h per (token, k)  */
+/* pair from fp32; the score, the expert outputs Y and out are as in the bf16 forward.          */
+/* Shape limits of the MXFP8 entry points: those above, with D and F multiples of 128.          */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Which weight moe_mxfp8_prepare_weight prepares. */
+enum { MOE_WEIGHT_W13 = 0, MOE_WEIGHT_W2 = 1 };
+
+/*
+ * Sizes of a prepared weight: *data_bytes of E4M3 codes and *scale_bytes of UE8M0 scales (host
+ * memory, caller-owned). Pure arithmetic.
+ *   MOE_WEIGHT_W13: data E*2F*D;  scales E * ceil(F/96) * (D/128) * 1024
+ *   MOE_WEIGHT_W2:  data E*D*F;   scales E * ceil(D/192) * (F/128) * 1024
+ */
+moe_status_t moe_mxfp8_weight_bytes(int32_t which, int32_t D, int32_t F, int32_t E, size_t *data_bytes,
+                                    size_t *scale_bytes);
+
+/*
+ * Prepares one expert weight for the MXFP8 forward (Dist-MoE's prepare_block_scaled_weight):
+ *   w       device bf16: w13 [E,2,F,D] (MOE_WEIGHT_W13) or w2 [E,D,F] (MOE_WEIGHT_W2)
+ *   data    device, data_bytes: E4M3 codes in w's own element order (w13 as [E*2F, D] rows, w2 as
+ *           [E*D, F] rows), each row quantized in blocks of 32 along its contiguous axis
+ *   scales  device, scale_bytes: the UE8M0 scales, grouped per GEMM tile so that one tile's
+ *           scales for 128 K values are one contiguous 1024-byte group. The scale of row n of
+ *           tile (e, j) and 32-block b along the row sits at byte
+ *             ((e * NT + j) * (C / 128) + b / 4) * 1024 + 512 * (n / 128)
+ *               + 16 * (n % 32) + 4 * ((n % 128) / 32) + b % 4
+ *           with C the row length. w13: NT = ceil(F/96), tile j holds gate rows f = 96j + n
+ *           (n < 96) then up rows f = 96j + n - 96; w2: NT = ceil(D/192), row d = 192j + n.
+ *           Bytes that belong to no row are 0.
+ * Deterministic: the same w gives the same bytes. Capacity: data_bytes and scale_bytes at least
+ * moe_mxfp8_weight_bytes' (MOE_ERR_WORKSPACE_TOO_SMALL otherwise). scales (here and in
+ * moe_routed_experts_fwd_mxfp8) must be 256-byte aligned.
+ */
+moe_status_t moe_mxfp8_prepare_weight(int32_t which, const void *w, int32_t D, int32_t F, int32_t E,
+                                      void *data, size_t data_bytes, void *scales, size_t scale_bytes,
+                                      moe_stream_t stream);
+
+/* Regions of the MXFP8 forward workspace, for moe_mxfp8_workspace_layout. Rp (padded rows) =
+ * 128 * (ceil(T*K/128) + min(E, T*K)): every expert's rows start on a 128-row boundary. */
+enum {
+    MOE_MXWS_STATUS = 0,       /* uint32 device status word (always at byte offset 0)           */
+    MOE_MXWS_COUNTS = 1,       /* int32 [E]                                                      */
+    MOE_MXWS_OFFSETS = 2,      /* int32 [E+1]                                                    */
+    MOE_MXWS_TILES = 3,        /* int32 [E+1] prefix of 128-row tiles: expert e's padded rows
+                                  start at 128 * tiles[e]                                        */
+    MOE_MXWS_TILES2 = 4,       /* int32 [E+1] (the same values; scratch of the routing scan)     */
+    MOE_MXWS_BLOCK_COUNTS = 5, /* int32 [(E+1)*B]                                                */
+    MOE_MXWS_BLOCK_BASES = 6,  /* int32 [(E+1)*B]                                                */
+    MOE_MXWS_PERM = 7,         /* int32 [T*K] routed row -> pair, as in the bf16 forward          */
+    MOE_MXWS_INV = 8,          /* int32 [T*K] pair -> routed row                                  */
+    MOE_MXWS_XQ = 9,           /* E4M3 [Rp, D] x rows: routed row offsets[e] + i of expert e at
+                                  padded row 128 * tiles[e] + i; zeros after each expert's rows  */
+    MOE_MXWS_XS = 10,          /* UE8M0 scales of XQ: padded row p, 32-block b at byte
+                                  ((p/128) * (D/128) + b/4) * 512 + 16 (p%32) + 4 ((p%128)/32) + b%4 */
+    MOE_MXWS_HQ = 11,          /* E4M3 [Rp, F] the SwiGLU output, same rows as XQ                */
+    MOE_MXWS_HS = 12,          /* UE8M0 scales of HQ, laid out as XS with F for D                */
+    MOE_MXWS_Y = 13,           /* bf16 [T*K, D] score-weighted expert output per pair            */
+    MOE_MXWS_TOTAL = 14,       /* total bytes (== moe_mxfp8_workspace_bytes)                     */
+    MOE_MXWS_REGIONS = 15
+};
+
+/* Bytes of device workspace that moe_routed_experts_fwd_mxfp8 needs (0 for T = 0 or sizes outside
+ * the MXFP8 shape limits). Pure arithmetic. */
+size_t moe_mxfp8_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K);
+
+/* Byte offsets of the MXFP8 workspace regions into region_offsets[MOE_MXWS_REGIONS] (host,
+ * caller-owned); each region starts on a 256-byte boundary. Pure arithmetic. */
+moe_status_t moe_mxfp8_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                        size_t *region_offsets);
+
+/*
+ * The MXFP8 forward: out as for moe_routed_experts_fwd, computed from MX-quantized x, w13, h and
+ * w2 with fp32 accumulation (block-scaled tcgen05 tensor-core GEMMs).
+ *   x, topk_ids, topk_scores, scores_dtype, out   as for moe_routed_experts_fwd
+ *   w13_data, w13_scales   device, as written by moe_mxfp8_prepare_weight(MOE_WEIGHT_W13)
+ *   w2_data, w2_scales     device, as written by moe_mxfp8_prepare_weight(MOE_WEIGHT_W2)
+ *   workspace  device, moe_mxfp8_workspace_bytes(T, D, F, E, K) bytes, 256-byte aligned; its
+ *              first 4 bytes are the device status word (moe_get_status)
+ * Deterministic. An id outside [0, E) sets MOE_DEV_BAD_EXPERT_ID and its pair contributes 0.
+ */
+moe_status_t moe_routed_experts_fwd_mxfp8(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                          int32_t scores_dtype, const void *w13_data, const void *w13_scales,
+                                          const void *w2_data, const void *w2_scales, void *out, int64_t T,
+                                          int32_t D, int32_t F, int32_t E, int32_t K, void *workspace,
+                                          size_t workspace_bytes, moe_stream_t stream);
+
 /* Capacity of the library-owned scratch of moe_routing_static_scratch, in int32 entries per
  * array: it serves sizes with (E + 1) * ceil(T*K / 2048) <= this value. */
 #define MOE_STATIC_SCRATCH_MAX_ENTRIES 262144

@@ -18,6 +18,13 @@ __all__ = [
     "moe_routed_experts_fwd_rmsnorm",
     "moe_bwd_workspace_bytes",
     "moe_routed_experts_bwd",
+    "moe_mxfp8_weight_bytes",
+    "moe_mxfp8_prepare_weight",
+    "moe_mxfp8_workspace_bytes",
+    "moe_mxfp8_workspace_layout",
+    "moe_routed_experts_fwd_mxfp8",
+    "MOE_WEIGHT_W13",
+    "MOE_WEIGHT_W2",
     "moe_get_status",
     "moe_status_string",
     "MoeError",

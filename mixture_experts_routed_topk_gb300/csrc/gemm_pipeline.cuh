@@ -2,11 +2,19 @@
 // grouped GEMM of the library (forward and backward), generic over a tile policy.
 //
 // One CTA per SM walks tiles c, c + grid, ... of a tile list the policy defines. Warp 0 issues TMA
-// loads into a 4-stage shared-memory ring (48 KB per stage: 16 KB of A, 32 KB of B), warp 1 owns
-// all 512 TMEM columns and issues tcgen05.mma from one thread into one of two 128 x 256 fp32
-// accumulators, warps 2-5 run the policy's epilogue from TMEM (one TMEM lane = one output row
-// per thread). full/empty mbarriers link producer and MMA; acc_full/acc_empty link MMA and
-// epilogue, so a tile's epilogue overlaps the next tile's mainloop. Every wait is bounded.
+// loads into a shared-memory ring of stages, warp 1 owns all 512 TMEM columns and issues
+// tcgen05.mma from one thread into one of two fp32 accumulators, warps 2-5 run the policy's
+// epilogue from TMEM (one TMEM lane = one output row per thread). full/empty mbarriers link
+// producer and MMA; acc_full/acc_empty link MMA and epilogue, so a tile's epilogue overlaps the
+// next tile's mainloop. Every wait is bounded.
+//
+// The policy's Shape fixes the ring and the MMA kind (Bf16Shape unless the policy names another):
+//   Bf16Shape: 4 stages of 16 KB A + 32 KB B (64 bf16 of K), 128 x 256 accumulators, kind::f16.
+//   Mxf8Shape: 4 stages of 16 KB A + 24 KB B (128 E4M3 of K) + their UE8M0 scale chunks (512 B
+//              for A's 128 rows, 1 KB for B's 192 rows), 128 x 192 accumulators (TMEM columns
+//              0..191 and 256..447), kind::mxf8f6f4 block-scaled; the MMA thread copies a stage's
+//              scales into that stage's 32-column TMEM slot (192, 224, 448, 480) with tcgen05.cp
+//              right before the stage's MMAs.
 //
 // A policy P provides
 //   struct P::Tile { int32_t kblocks; ... }              one tile's coordinates and K steps
@@ -16,9 +24,10 @@
 //   __device__ static Tile decode(int32_t tile, const GemmArgs&)
 //   __device__ static void load(const Tile&, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
 //                               const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs&)
+//        (block-scaled shapes: load(t, kb, sa, sb, sf, bar, ta, tb, args), sf = the scale chunks)
 //   __device__ static void epilogue(const Tile&, uint32_t taddr, int row, uint4* stage,
 //                                   const GemmArgs&)          (taddr = this warp's TMEM lanes)
-// Every load() must deliver exactly kStageBytes into the stage.
+// Every load() must deliver exactly the shape's kTxBytes into the stage.
 #pragma once
 
 #include <cuda.h>
@@ -26,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "moe_internal.cuh"
 #include "ptx_sm103.cuh"
@@ -39,6 +49,43 @@ constexpr int kBBytes = kBRows * kBK * 2;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
+constexpr int kMaxStages = 8;
+
+struct Bf16Shape {
+    static constexpr int kStages = moe::kStages;
+    static constexpr int kABytes = moe::kABytes, kBBytes = moe::kBBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;  // a multiple of 1024
+    static constexpr int kTxBytes = kABytes + kBBytes;
+    static constexpr int kAccCols = moe::kAccCols;
+    static constexpr bool kBlockScaled = false;
+};
+
+// E4M3 operands with UE8M0 block scales: kMxBK = 128 K elements (128 bytes, one swizzled row) per
+// stage, kMxBN = 192 accumulator columns per tile.
+struct Mxf8Shape {
+    static constexpr int kStages = 4;
+    static constexpr int kABytes = kBM * kMxBK;         // 16 KB
+    static constexpr int kBBytes = kMxBN * kMxBK;       // 24 KB
+    static constexpr int kSfaBytes = 512, kSfbBytes = 1024;
+    static constexpr int kStageBytes = 43008;           // 16 + 24 + 1.5 KB, rounded up to 1024
+    static constexpr int kTxBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    static constexpr int kAccCols = 256;  // accumulators at TMEM columns 0 and 256, 192 wide each
+    static constexpr bool kBlockScaled = true;
+    // Scale slot of stage s (32 columns: A's scales at +0, B's at +16): in the two gaps after the
+    // accumulators, columns 192..255 and 448..511.
+    __device__ static constexpr uint32_t sf_slot_col(uint32_t s) { return (s & 2u) * 128u + 192u + 32u * (s & 1u); }
+};
+static_assert(Mxf8Shape::kStageBytes % 1024 == 0 && Mxf8Shape::kTxBytes <= Mxf8Shape::kStageBytes, "stage");
+static_assert(Mxf8Shape::kStages == 4 && kMxBN + 64 == Mxf8Shape::kAccCols, "four 32-column scale slots in the gaps");
+
+template <class P, class = void>
+struct ShapeOf {
+    using type = Bf16Shape;
+};
+template <class P>
+struct ShapeOf<P, std::void_t<typename P::Shape>> {
+    using type = typename P::Shape;
+};
 constexpr int kGemmThreads = 192;
 constexpr int kEpilogueThreads = 128;
 constexpr int kMnBoxBytes = 64 * kBK * 2;   // one 64 (M or N) x 64 (K) MN-major box: 8 KB
@@ -49,8 +96,8 @@ constexpr int kStageRowU4 = 9;  // 144-byte row stride in 16-byte units
 constexpr int kEpilogueStagingBytes = (kEpilogueThreads / 32) * 32 * kStageRowU4 * 16;
 
 struct alignas(8) PipeState {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -58,8 +105,11 @@ struct alignas(8) PipeState {
     int abort;
 };
 
-constexpr size_t kGemmSmemBytes =
-    1024 + static_cast<size_t>(kStages) * kStageBytes + kEpilogueStagingBytes + sizeof(PipeState);
+template <class S>
+constexpr size_t gemm_smem_bytes() {
+    return 1024 + static_cast<size_t>(S::kStages) * S::kStageBytes + kEpilogueStagingBytes + sizeof(PipeState);
+}
+static_assert(gemm_smem_bytes<Mxf8Shape>() <= 232448 && gemm_smem_bytes<Bf16Shape>() <= 232448, "smem");
 
 // Everything any policy needs (each policy reads its own fields).
 struct GemmArgs {
@@ -81,6 +131,12 @@ struct GemmArgs {
     const __nv_bfloat16* in0;  // extra epilogue input
     float* fout;             // fp32 policy output
     uint32_t* status;
+    // block-scaled (MXFP8) policies
+    const uint8_t* sf_a;     // A's UE8M0 scale chunks
+    const uint8_t* sf_b;     // B's UE8M0 scale chunks
+    uint8_t* q_out;          // E4M3 output codes
+    uint8_t* sf_out;         // the output's scale chunks
+    int32_t ntn;             // column tiles per row tile
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -159,19 +215,20 @@ template <class P>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const GemmArgs args) {
+    using S = typename ShapeOf<P>::type;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared address space
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     uint8_t* smem = smem_raw + pad;
-    uint4* staging = reinterpret_cast<uint4*>(smem + kStages * kStageBytes);
-    PipeState* ps = reinterpret_cast<PipeState*>(smem + kStages * kStageBytes + kEpilogueStagingBytes);
+    uint4* staging = reinterpret_cast<uint4*>(smem + S::kStages * S::kStageBytes);
+    PipeState* ps = reinterpret_cast<PipeState*>(smem + S::kStages * S::kStageBytes + kEpilogueStagingBytes);
     volatile int* abort_flag = &ps->abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S::kStages; ++s) {
             mbar_init(&ps->full[s], 1);
             mbar_init(&ps->empty[s], 1);
         }
@@ -207,15 +264,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int32_t tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
                 const typename P::Tile t = P::decode(tile, args);
                 for (int32_t kb = 0; kb < t.kblocks; ++kb, ++it) {
-                    const uint32_t s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
+                    const uint32_t s = it % S::kStages;
+                    const uint32_t ph = (it / S::kStages) & 1u;
                     if (!mbar_wait(&ps->empty[s], ph ^ 1u, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + s * kStageBytes;
-                    mbar_arrive_expect_tx(&ps->full[s], kStageBytes);
-                    P::load(t, kb, sa, sa + kABytes, &ps->full[s], &tmap_a, &tmap_b, args);
+                    uint8_t* sa = smem + s * S::kStageBytes;
+                    mbar_arrive_expect_tx(&ps->full[s], S::kTxBytes);
+                    if constexpr (S::kBlockScaled)
+                        P::load(t, kb, sa, sa + S::kABytes, sa + S::kABytes + S::kBBytes, &ps->full[s], &tmap_a,
+                                &tmap_b, args);
+                    else
+                        P::load(t, kb, sa, sa + S::kABytes, &ps->full[s], &tmap_a, &tmap_b, args);
                 }
             }
             if (!ok) {
@@ -239,21 +300,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 tcgen05_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + acc * kAccCols;
+                const uint32_t d_tmem = tmem_base + acc * S::kAccCols;
                 for (int32_t kb = 0; kb < t.kblocks; ++kb, ++it) {
-                    const uint32_t s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
+                    const uint32_t s = it % S::kStages;
+                    const uint32_t ph = (it / S::kStages) & 1u;
                     if (!mbar_wait(&ps->full[s], ph, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
                         ok = false;
                         break;
                     }
                     tcgen05_fence_after_sync();
-                    const uint32_t a0 = smem_addr(smem + s * kStageBytes);
-                    const uint32_t b0 = a0 + kABytes;
+                    const uint32_t a0 = smem_addr(smem + s * S::kStageBytes);
+                    const uint32_t b0 = a0 + S::kABytes;
+                    if constexpr (S::kBlockScaled) {
+                        // this stage's scales into its TMEM slot; the slot's previous reader (the MMAs
+                        // of stage use it - kStages) completed before the stage was refilled
+                        const uint32_t sf0 = b0 + S::kBBytes;
+                        const uint32_t sfa_t = tmem_base + S::sf_slot_col(s);
+                        const uint32_t sfb_t = sfa_t + 16u;
+                        tmem_cp_scale_chunk(sfa_t, sf_chunk_desc(sf0));
+                        tmem_cp_scale_chunk(sfb_t, sf_chunk_desc(sf0 + 512));
+                        tmem_cp_scale_chunk(sfb_t + 4u, sf_chunk_desc(sf0 + 1024));
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_ss(d_tmem, operand_desc<P::kAMnMajor>(a0, kk), operand_desc<P::kBMnMajor>(b0, kk),
-                                    P::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kMxBK / 32; ++kk)
+                            mma_mxf8_ss(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
+                                        P::kIdesc | mxf8_ids(kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16_ss(d_tmem, operand_desc<P::kAMnMajor>(a0, kk),
+                                        operand_desc<P::kBMnMajor>(b0, kk), P::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
                     mma_commit(&ps->empty[s]);  // frees the stage once these MMAs have read it
                 }
                 if (!ok) break;
@@ -280,7 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t aph = (tcount >> 1) & 1u;
             if (!warp_wait(&ps->acc_full[acc], aph, abort_flag, args.status)) break;
             tcgen05_fence_after_sync();
-            P::epilogue(t, tmem_base + lane_base + acc * kAccCols, row_in_tile, wstage, args);
+            P::epilogue(t, tmem_base + lane_base + acc * S::kAccCols, row_in_tile, wstage, args);
             tcgen05_fence_before_sync();
             mbar_arrive(&ps->acc_empty[acc]);
         }
@@ -302,11 +378,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                uint32_t box_rows);
 
+// The same for a byte tensor (E4M3 codes): inner and box_inner count bytes.
+bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows);
+
 int sm_count_grid(int64_t max_tiles, int sm_count);
 
 template <class P>
 moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
                          cudaStream_t stream) {
+    constexpr size_t kGemmSmemBytes = gemm_smem_bytes<typename ShapeOf<P>::type>();
     constexpr int kMaxDevices = 64;
     static std::atomic<bool> attr_set[kMaxDevices];
     int dev = 0;

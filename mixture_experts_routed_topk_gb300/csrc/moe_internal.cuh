@@ -26,6 +26,13 @@ constexpr int kBN1 = 128;  // f values per gate/up tile
 constexpr int kBN2 = 256;  // output columns per down tile
 constexpr int kBK = 64;
 
+// MXFP8 grouped GEMM tiles: 128 rows x 192 accumulator columns, K in 128-element (128-byte)
+// steps. A gate/up tile holds 96 gate and the same 96 up columns of one f range.
+constexpr int kMxBK = 128;
+constexpr int kMxBN = 192;
+constexpr int kMxGateUpF = kMxBN / 2;  // 96 f values per gate/up tile
+constexpr int kMxDownN = kMxBN;        // 192 output columns per down tile
+
 // Host: launches `kernel` with programmatic stream serialization, so its launch and prologue may
 // overlap the tail of the previous kernel on the stream. Every kernel launched this way calls
 // griddep_wait() before its first global memory access, so the stream order of memory effects is
@@ -134,6 +141,32 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream);
 
 moe_status_t launch_combine(const void* y, const int32_t* ids, int64_t T, int32_t D, int32_t E, int32_t K,
                             void* out, int sm_count, cudaStream_t stream);
+
+// MXFP8 forward (mxfp8.cu). Weights are prepared once (E4M3 codes in the weight's own row order,
+// UE8M0 scales grouped per GEMM tile); every pointer below is device memory.
+// which = 0: w13 [E, 2F, D]; which = 1: w2 [E, D, F]. scales is cleared, then filled.
+moe_status_t launch_mx_prepare_weight(int which, const void* w, int32_t D, int32_t F, int32_t E, void* data,
+                                      void* scales, size_t scale_bytes, int sm_count, cudaStream_t stream);
+
+struct MxProblem {
+    int64_t T;
+    int32_t D, F, E, K;
+    const void* x;
+    const int32_t* ids;
+    const void* scores;
+    int32_t scores_dtype;
+    const void *w13q, *w13s, *w2q, *w2s;
+    void* out;
+    // workspace
+    uint32_t* status;
+    int32_t *counts, *offsets, *tiles1, *tiles2, *block_counts, *block_bases, *perm, *inv;
+    uint8_t *xq, *xs, *hq, *hs;
+    void* y;
+    int nblk;
+    int64_t padded_rows;  // capacity of XQ / HQ: 128 * (ceil(R / 128) + min(E, R))
+    int sm_count;
+};
+moe_status_t launch_mx_forward(const MxProblem& p, cudaStream_t stream);
 
 // The combine of the route-wise RMSNorm variant: out[t] = sum_k s * y / sqrt(mean(y^2) + eps).
 moe_status_t launch_combine_rmsnorm(const void* y, const int32_t* ids, const void* scores, int32_t scores_dtype,

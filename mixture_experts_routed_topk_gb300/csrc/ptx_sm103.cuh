@@ -1,6 +1,7 @@
 // ptx_sm103.cuh -- inline-PTX wrappers for the Blackwell (sm_103a) asynchronous machinery used
 // by the grouped GEMMs: mbarriers (with bounded waits), TMA tensor loads, tcgen05 tensor-memory
-// allocation, tcgen05.mma (bf16 in, fp32 accumulate in TMEM), tcgen05.commit and tcgen05.ld.
+// allocation, tcgen05.mma (bf16 in, or block-scaled E4M3 in with tcgen05.cp of the scales; fp32
+// accumulate in TMEM), tcgen05.commit and tcgen05.ld.
 //
 // Written from the public PTX ISA (tcgen05 / cp.async.bulk.tensor / mbarrier chapters). Every wait
 // here is bounded: it gives up after kWaitTimeoutNs of wall time, sets MOE_DEV_TIMEOUT in the
@@ -106,6 +107,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both addresses 16-byte aligned),
+// completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------------------------ tensor memory
 
 // Allocates `ncols` TMEM columns (power of two, >= 32) for this CTA; the whole warp must execute
@@ -182,6 +192,54 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// ------------------------------------------------------------------- block-scaled (MXFP8) MMA
+//
+// Scale factors live in TMEM. A 512-byte shared-memory chunk holds the UE8M0 scales of 128 rows
+// (of A, or of B's N dimension) for four consecutive 32-element K blocks: row r, block k at byte
+// 16 * (r % 32) + 4 * (r / 32) + k. tcgen05.cp .32x128b.warpx4 copies it as 32 rows of 16 bytes
+// into columns c .. c+3 of every 32-lane quarter of TMEM, so the scale of row r sits in column
+// c + r / 32, byte k, of lane r % 32 of each quarter; the MMA's scale-factor id picks byte k. A
+// 256-row operand (B with N > 128) takes two chunks in columns c .. c+7.
+
+// Shared-memory descriptor of one such chunk: no swizzle, 8-row core matrices of 16-byte rows
+// stacked 128 bytes apart (stride-dimension byte offset 128), descriptor version 1.
+__device__ __forceinline__ uint64_t sf_chunk_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
+// Copies one 512-byte scale chunk from shared memory to TMEM columns taddr .. taddr+3 of all four
+// lane quarters. Issued by one thread; ordered before the tcgen05.mma it issues afterwards.
+__device__ __forceinline__ void tmem_cp_scale_chunk(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma .kind::mxf8f6f4 with A and B E4M3 (format 0 at [7,10) and
+// [10,13)), both K-major, N >> 3 at [17,23), UE8M0 scales (bit 23), M >> 4 at [24,29). The
+// scale-factor ids (B at [4,6), A at [29,31)) are added per K step by mxf8_ids().
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N) {
+    return (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t mxf8_ids(int k) {
+    return (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+}
+
+// D[tmem] (+)= (A * 2^sfa) (B * 2^sfb)^T for one M x N x 32 step of E4M3 operands with one UE8M0
+// scale per row and 32 K elements (scale_vec::1X), issued by a single thread.
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 

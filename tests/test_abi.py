@@ -142,3 +142,68 @@ def test_binding_region_list_matches_header():
     text = open(HEADER).read()
     n = int(re.search(r"MOE_WS_REGIONS\s*=\s*(\d+)", text).group(1))
     assert len(binding.WS_REGIONS) == n
+
+
+def mx_fwd(lib, **kw):
+    a = dict(x=FAKE, ids=FAKE, scores=FAKE, sd=0, w13q=FAKE, w13s=FAKE, w2q=FAKE, w2s=FAKE, out=FAKE,
+             T=16, D=256, F=256, E=8, K=2, ws=FAKE, wsb=1 << 40)
+    a.update(kw)
+    v = ctypes.c_void_p
+    return lib.moe_routed_experts_fwd_mxfp8(
+        v(a["x"]), v(a["ids"]), v(a["scores"]), a["sd"], v(a["w13q"]), v(a["w13s"]), v(a["w2q"]), v(a["w2s"]),
+        v(a["out"]), a["T"], a["D"], a["F"], a["E"], a["K"], v(a["ws"]), a["wsb"], None)
+
+
+def test_mxfp8_host_validation_needs_no_gpu(lib):
+    assert mx_fwd(lib, T=0) == OK
+    assert mx_fwd(lib, T=-1) == INVALID
+    assert mx_fwd(lib, sd=2) == INVALID
+    assert mx_fwd(lib, w13s=0) == INVALID
+    assert mx_fwd(lib, w2q=0) == INVALID
+    assert mx_fwd(lib, D=192) == SHAPE  # a multiple of 64 but not of 128
+    assert mx_fwd(lib, F=320) == SHAPE
+    assert mx_fwd(lib, E=4097) == SHAPE
+    assert mx_fwd(lib, w13s=FAKE + 16) == MISALIGNED  # scales must be 256-byte aligned
+    assert mx_fwd(lib, w2q=FAKE + 8) == MISALIGNED
+    assert mx_fwd(lib, ws=FAKE + 64) == MISALIGNED
+    need = binding.moe_mxfp8_workspace_bytes(16, 256, 256, 8, 2)
+    assert mx_fwd(lib, wsb=need - 1) == WS_SMALL
+    v = ctypes.c_void_p
+    prep = lambda **kw: lib.moe_mxfp8_prepare_weight(
+        kw.get("which", 0), v(kw.get("w", FAKE)), kw.get("D", 256), kw.get("F", 256), kw.get("E", 8),
+        v(kw.get("data", FAKE)), kw.get("nd", 1 << 40), v(kw.get("sc", FAKE)), kw.get("ns", 1 << 40), None)
+    assert prep(which=2) == INVALID
+    assert prep(w=0) == INVALID
+    assert prep(D=64) == SHAPE
+    assert prep(sc=FAKE + 16) == MISALIGNED
+    nd, ns = binding.moe_mxfp8_weight_bytes(binding.MOE_WEIGHT_W2, 256, 256, 8)
+    assert prep(which=1, nd=nd - 1) == WS_SMALL
+    assert prep(which=1, ns=ns - 1) == WS_SMALL
+
+
+@pytest.mark.parametrize("dims", [(16, 256, 256, 8, 2), (4096, 2048, 1408, 64, 6), (64, 7168, 2048, 256, 8),
+                                  (16384, 7168, 2048, 256, 8), (16384, 4096, 1536, 128, 8), (1, 128, 128, 1, 1)])
+def test_mxfp8_sizes_and_layout(lib, dims):
+    T, D, F, E, K = dims
+    R = T * K
+    nd, ns = binding.moe_mxfp8_weight_bytes(binding.MOE_WEIGHT_W13, D, F, E)
+    assert nd == E * 2 * F * D and ns == E * -(-F // 96) * (D // 128) * 1024
+    nd, ns = binding.moe_mxfp8_weight_bytes(binding.MOE_WEIGHT_W2, D, F, E)
+    assert nd == E * D * F and ns == E * -(-D // 192) * (F // 128) * 1024
+    lay = binding.moe_mxfp8_workspace_layout(*dims)
+    rp = 128 * (-(-R // 128) + min(E, R))
+    sizes = {"status": 4, "counts": 4 * E, "offsets": 4 * (E + 1), "tiles": 4 * (E + 1), "perm": 4 * R,
+             "inv": 4 * R, "xq": rp * D, "xs": rp * D // 32, "hq": rp * F, "hs": rp * F // 32, "y": 2 * R * D}
+    names = list(binding.MXWS_REGIONS)
+    for i, name in enumerate(names[:-1]):
+        assert lay[name] % 256 == 0
+        if name in sizes:
+            assert lay[names[i + 1]] - lay[name] >= sizes[name], name
+    assert lay["status"] == 0
+    assert lay["total"] == binding.moe_mxfp8_workspace_bytes(*dims)
+
+
+def test_binding_mx_region_list_matches_header():
+    text = open(HEADER).read()
+    n = int(re.search(r"MOE_MXWS_REGIONS\s*=\s*(\d+)", text).group(1))
+    assert len(binding.MXWS_REGIONS) == n

@@ -6,6 +6,10 @@ row gather), the gate/up grouped GEMM with SwiGLU, the down grouped GEMM with th
 weighting, and the combine -- through the C ABI, on inputs already resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+                    [--precision bf16|mxfp8] [--pass fwd|bwd]
+
+--precision mxfp8 runs the block-scaled forward (E4M3 operands with UE8M0 scales, weights prepared
+once before the timed region, activations quantized inside each step).
 
 Prints ONE JSON line (rank 0). Under torchrun each rank runs its own replica of the workload
 (tokens drawn with a rank-specific seed, the same weights): the path has no exchange step on one
@@ -50,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--config", default="medium", choices=["tiny", "medium", "decode", "large", "skewed"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8"],
+                   help="forward operands: bf16, or MXFP8 E4M3 with prepared weights")
     p.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
                    help="fwd: the forward layer (the headline); bwd: its backward pass (one call per step)")
     p.add_argument("--seed", type=int, default=0)
@@ -112,9 +118,18 @@ def measured_peaks() -> tuple[dict, str]:
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_costs(T, D, F, E, K, touched):
-    """Algorithmic flops and bytes per launch of each stage (tile padding not counted)."""
+def kernel_costs(T, D, F, E, K, touched, mx=False):
+    """Algorithmic flops and bytes per launch of each stage (tile padding not counted). With mx the
+    operands are E4M3 bytes plus one UE8M0 scale byte per 32 (1 + 1/32 bytes per element)."""
     R = T * K
+    if mx:
+        q = 1.0 + 1.0 / 32
+        return {
+            "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + R * D * 2 + R * D * q},
+            "gemm1_swiglu": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * q + R * D * q + R * F * q},
+            "gemm2_score": {"flops": 2 * R * D * F, "bytes": touched * D * F * q + R * F * q + R * D * 2 + R * 8},
+            "combine": {"flops": 0, "bytes": R * D * 2 + T * D * 2 + R * 4},
+        }
     return {
         "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + 2 * R * D * 2},
         "gemm1_swiglu": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * 2 + R * D * 2 + R * F * 2},
@@ -123,20 +138,28 @@ def kernel_costs(T, D, F, E, K, touched):
     }
 
 
-def path_costs(T, D, F, E, K, touched):
+def path_costs(T, D, F, E, K, touched, mx=False):
     """The layer's algorithmic flops and bytes: touched experts' weights, x, out, ids, scores."""
-    return 6 * T * K * D * F, touched * 3 * F * D * 2 + 2 * T * D * 2 + T * K * 8
+    wbytes = (1.0 + 1.0 / 32) if mx else 2
+    return 6 * T * K * D * F, touched * 3 * F * D * wbytes + 2 * T * D * 2 + T * K * 8
 
 
-def roofline_entry(name, costs, seconds, peaks, sustained, traffic):
+# Dense fp8 (E4M3, block-scaled) over dense bf16 tensor throughput, nominal (4.5 / 2.25 PFLOP/s).
+FP8_OVER_BF16 = 2.0
+
+
+def roofline_entry(name, costs, seconds, peaks, sustained, traffic, tensor_scale=1.0):
+    """tensor_scale multiplies the measured bf16 peak for another operand type (FP8_OVER_BF16)."""
     c = costs[name]
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ridge = tensor_scale * peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if c["flops"] > 0 and c["flops"] / max(c["bytes"], 1) >= ridge:
-        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        peak = tensor_scale * (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"])
         achieved = c["flops"] / seconds / 1e12
-        return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": name,
-                "peak_kind": "sustained" if sustained else "burst"}
+        kind = "sustained" if sustained else "burst"
+        if tensor_scale != 1.0:
+            kind += f" bf16 x {tensor_scale:g} (fp8/bf16 nominal ratio)"
+        return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": name, "peak_kind": kind}
     achieved = c["bytes"] / seconds / 1e9
     peak = peaks["hbm_gbs"]
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -147,6 +170,7 @@ def kernel_source_hash() -> str:
     """Hash of the grouped-GEMM sources; a recorded DRAM traffic is only valid for this hash."""
     h = hashlib.sha256()
     for rel in ("mixture_experts_routed_topk_gb300/csrc/grouped_gemm.cu",
+                "mixture_experts_routed_topk_gb300/csrc/mxfp8.cu",
                 "mixture_experts_routed_topk_gb300/csrc/gemm_pipeline.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/ptx_sm103.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/routing.cu",
@@ -279,18 +303,28 @@ def time_oracle(sample, nthreads: int) -> float:
     import oracle
 
     t0 = time.perf_counter()
-    oracle.routed_experts(sample["x"], sample["ids"], sample["scores"], sample["w13"], sample["w2"],
-                          nthreads=nthreads)
+    if "w13_mx" in sample:
+        oracle.routed_experts_mxfp8(sample["x"], sample["ids"], sample["scores"], sample["w13_mx"],
+                                    sample["w2_mx"], nthreads=nthreads)
+    else:
+        oracle.routed_experts(sample["x"], sample["ids"], sample["scores"], sample["w13"], sample["w2"],
+                              nthreads=nthreads)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(d, wl, name: str, target_s: float) -> dict:
+def cpu_baseline(d, wl, name: str, target_s: float, mx: bool = False) -> dict:
     """The oracle as it stands on the host cores: a bounded token sample, repeated to fill about
-    target_s seconds; tokens/s = tokens processed / seconds."""
+    target_s seconds; tokens/s = tokens processed / seconds. With mx, the oracle's MXFP8 forward on
+    weights the oracle quantized beforehand (not timed, as the weights are prepared once)."""
     cores = os.cpu_count() or 1
     ids_host = d["topk_ids"].cpu().numpy()
-    n_tok = bounded_tokens(ids_host, wl, oracle_tokens_for(target_s, wl, cores))
+    n_tok = bounded_tokens(ids_host, wl, oracle_tokens_for(target_s, wl, cores, 0.35 if mx else 0.7))
     sample = oracle_sample(d, n_tok)
+    if mx:
+        import oracle
+
+        sample["w13_mx"] = oracle.mx_quantize_rows(sample["w13"])
+        sample["w2_mx"] = oracle.mx_quantize_rows(sample["w2"])
     secs = [time_oracle(sample, cores)]
     reps = max(1, min(100, int(target_s / max(secs[0], 1e-6))))
     secs += [time_oracle(sample, cores) for _ in range(reps - 1)]
@@ -324,12 +358,26 @@ def run_ours(args, rank, world, local_rank):
     scores = W.make_scores(T, K, wl.scores, rseed, device)
     w13, w2 = W.make_weights(E, D, F, args.seed, device)
     dims = (T, D, F, E, K)
-    ws = binding.alloc_workspace(binding.moe_workspace_bytes(*dims), device)
+    mx = args.precision == "mxfp8"
+    if mx:  # prepared once, as the pages prepare block-scaled weights before execution
+        w13_mx = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W13, w13)
+        w2_mx = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W2, w2)
+        ws = binding.alloc_workspace(binding.moe_mxfp8_workspace_bytes(*dims), device)
+    else:
+        ws = binding.alloc_workspace(binding.moe_workspace_bytes(*dims), device)
     out = torch.empty((T, D), dtype=torch.bfloat16, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
     def step(ev=None):
+        if mx:
+            for s in range(binding.MX_STAGES):
+                if ev is not None:
+                    ev[s].record(stream)
+                binding.moe_fwd_mxfp8_stages(x, ids, scores, w13_mx, w2_mx, out, ws, (F, E), s, s + 1, stream)
+            if ev is not None:
+                ev[binding.MX_STAGES].record(stream)
+            return
         if ev is not None:
             ev[0].record(stream)
         binding.moe_fwd_dispatch(x, ids, dims, ws, stream)
@@ -352,7 +400,7 @@ def run_ours(args, rank, world, local_rank):
     status = binding.moe_get_status(ws, stream)
     if status != 0:
         raise RuntimeError(f"device status bits {status:#x} after warm-up")
-    counts = binding.moe_workspace_layout(*dims)
+    counts = binding.moe_mxfp8_workspace_layout(*dims) if mx else binding.moe_workspace_layout(*dims)
     cnt = ws[counts["counts"]:counts["counts"] + 4 * E].view(torch.int32)
     touched = int((cnt > 0).sum().item())
 
@@ -413,7 +461,11 @@ def run_ours(args, rank, world, local_rank):
             stream.wait_event(uploaded[b])
             if i >= 2:
                 stream.wait_event(read_back[b])  # out_d[b] of step i-2 has been read back
-            binding.moe_routed_experts_fwd(x_d[b], ids_d[b], scores_d[b], w13, w2, out_d[b], ws, stream)
+            if mx:
+                binding.moe_routed_experts_fwd_mxfp8(x_d[b], ids_d[b], scores_d[b], w13_mx, w2_mx, out_d[b], ws,
+                                                     (F, E), stream)
+            else:
+                binding.moe_routed_experts_fwd(x_d[b], ids_d[b], scores_d[b], w13, w2, out_d[b], ws, stream)
             computed[b].record(stream)
             if i + 1 < n:
                 upload(i + 1)  # overlaps this step's compute
@@ -445,22 +497,23 @@ def run_ours(args, rank, world, local_rank):
         return
 
     peaks, peak_src = measured_peaks()
-    costs = kernel_costs(T, D, F, E, K, touched)
+    costs = kernel_costs(T, D, F, E, K, touched, mx)
     mean_stage = {s: statistics.mean(v) for s, v in stage_ms.items()}
     dominant = max(mean_stage, key=mean_stage.get)
     ms_per_step = total_s * 1e3 / args.steps
     sustained = ms_per_step * args.steps > 2000.0  # a seconds-long loop runs under the power cap
+    tensor_scale = FP8_OVER_BF16 if mx else 1.0
     roof = roofline_entry(dominant, costs, mean_stage[dominant] / 1e3, peaks, sustained,
-                          recorded_traffic(args.config, dominant))
+                          recorded_traffic(args.config, ("mx_" if mx else "") + dominant), tensor_scale)
     roof["peak_source"] = peak_src
-    flops, alg_bytes = path_costs(T, D, F, E, K, touched)
+    flops, alg_bytes = path_costs(T, D, F, E, K, touched, mx)
     step_s = ms_per_step / 1e3
-    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
+    t_roof = max(flops / (tensor_scale * peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
 
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline({"x": x, "topk_ids": ids, "topk_scores": scores, "w13": w13, "w2": w2}, wl,
-                           args.config, args.cpu_seconds)
+                           args.config, args.cpu_seconds, mx)
 
     line = assemble_line(
         metric=METRIC,
@@ -473,9 +526,10 @@ def run_ours(args, rank, world, local_rank):
         higher_is_better=True,
         scaling="weak",
         vs_baseline=None,
-        dtype="bf16",
+        dtype="mxfp8-e4m3" if mx else "bf16",
         data="synthetic",
         config={"workload": args.config if not args.tokens else f"{args.config} (T={T})", "T": T, "D": D, "F": F,
+                "precision": args.precision,
                 "E": E, "K": K, "routing": wl.routing, "experts_touched": touched, "global_batch": T * world, "parallelism": f"replicas{world}",
                 "l2": "flushed between steps (512 MB write)", "seed": args.seed},
         tflops=round(world * flops / step_s / 1e12, 2),
@@ -597,12 +651,16 @@ def run_reference(args, rank, world, local_rank):
     x = W.make_x(T, D, args.seed, dev)
     ids = W.make_topk_ids(T, E, K, wl.routing, args.seed, dev)
     scores = W.make_scores(T, K, wl.scores, args.seed, dev)
-    n_tok = bounded_tokens(ids.cpu().numpy(), wl, oracle_tokens_for(per_step_s, wl, cores))
+    mx = args.precision == "mxfp8"
+    n_tok = bounded_tokens(ids.cpu().numpy(), wl, oracle_tokens_for(per_step_s, wl, cores, 0.35 if mx else 0.7))
     first = ids[:n_tok].cpu()
     experts = sorted(set(first[(first >= 0) & (first < E)].tolist()))
     w13, w2 = W.make_weights(E, D, F, args.seed, dev, experts=experts)
     sample = oracle_sample({"x": x, "topk_ids": ids, "topk_scores": scores, "w13": w13, "w2": w2}, n_tok)
     del w13, w2
+    if mx:  # weights prepared once, outside the timed steps
+        sample["w13_mx"] = oracle.mx_quantize_rows(sample["w13"])
+        sample["w2_mx"] = oracle.mx_quantize_rows(sample["w2"])
     for _ in range(max(args.warmup, 0)):
         time_oracle(sample, cores)
     secs = [time_oracle(sample, cores) for _ in range(args.steps)]
@@ -615,7 +673,7 @@ def run_reference(args, rank, world, local_rank):
         warmup=args.warmup, ms_per_step=round(total * 1e3 / args.steps, 3), higher_is_better=True,
         scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
         config={"workload": args.config, "T": T, "D": D, "F": F, "E": E, "K": K, "routing": wl.routing,
-                "sample_tokens": n_tok},
+                "precision": args.precision, "sample_tokens": n_tok},
         cpu_baseline={"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
         e2e={"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     ), flush=True)
@@ -627,6 +685,8 @@ def main(argv=None):
     if args.impl == "reference":
         run_reference(args, rank, world, local_rank)
     elif args.which == "bwd":
+        if args.precision != "bf16":
+            raise SystemExit("the backward pass runs in bf16 only")
         run_ours_bwd(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)

@@ -330,6 +330,27 @@ moe_status_t moe_routed_experts_fwd_mxfp8(const void *x, const int32_t *topk_ids
                                           int32_t D, int32_t F, int32_t E, int32_t K, void *workspace,
                                           size_t workspace_bytes, moe_stream_t stream);
 
+/* Stages of the MXFP8 forward, for moe_fwd_mxfp8_stages. */
+enum {
+    MOE_MX_STAGE_DISPATCH = 0, /* status word cleared, routing, x rows gathered and quantized (XQ) */
+    MOE_MX_STAGE_GATE_UP = 1,  /* gate/up GEMM, SwiGLU, H quantized (HQ)                             */
+    MOE_MX_STAGE_DOWN = 2,     /* down GEMM with the score (Y)                                        */
+    MOE_MX_STAGE_COMBINE = 3,  /* out from Y                                                          */
+    MOE_MX_STAGES = 4
+};
+
+/*
+ * Stages stage_begin .. stage_end-1 of moe_routed_experts_fwd_mxfp8 (0 <= stage_begin <= stage_end
+ * <= MOE_MX_STAGES; the full range is that call). Arguments as for moe_routed_experts_fwd_mxfp8;
+ * a stage reads what the earlier stages left in the same workspace, so stages run in order on
+ * one stream. Lets a caller time each stage with events or read an intermediate region.
+ */
+moe_status_t moe_fwd_mxfp8_stages(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                  int32_t scores_dtype, const void *w13_data, const void *w13_scales,
+                                  const void *w2_data, const void *w2_scales, void *out, int64_t T, int32_t D,
+                                  int32_t F, int32_t E, int32_t K, int32_t stage_begin, int32_t stage_end,
+                                  void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Capacity of the library-owned scratch of moe_routing_static_scratch, in int32 entries per
  * array: it serves sizes with (E + 1) * ceil(T*K / 2048) <= this value. */
 #define MOE_STATIC_SCRATCH_MAX_ENTRIES 262144

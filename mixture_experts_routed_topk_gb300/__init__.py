@@ -23,6 +23,7 @@ __all__ = [
     "moe_mxfp8_workspace_bytes",
     "moe_mxfp8_workspace_layout",
     "moe_routed_experts_fwd_mxfp8",
+    "moe_fwd_mxfp8_stages",
     "MOE_WEIGHT_W13",
     "MOE_WEIGHT_W2",
     "moe_get_status",

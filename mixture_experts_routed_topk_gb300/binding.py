@@ -87,6 +87,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "moe_mxfp8_workspace_layout": ([i64, i32, i32, i32, i32, vp], ctypes.c_int),
             "moe_routed_experts_fwd_mxfp8": (
                 [vp, vp, vp, i32, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_fwd_mxfp8_stages": (
+                [vp, vp, vp, i32, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -359,12 +361,21 @@ def moe_mxfp8_workspace_layout(T: int, D: int, F: int, E: int, K: int) -> dict:
     return dict(zip(MXWS_REGIONS, (int(v) for v in arr)))
 
 
+MX_STAGES = 4
+
+
 def moe_routed_experts_fwd_mxfp8(x, topk_ids, topk_scores, w13_mx, w2_mx, out, workspace, dims_FE=None,
                                  stream=None) -> None:
     """The MXFP8 forward. w13_mx, w2_mx: (data, scales) from moe_mxfp8_prepare_weight.
 
     dims_FE = (F, E); the prepared weights are flat byte tensors, so F and E come from here.
     """
+    moe_fwd_mxfp8_stages(x, topk_ids, topk_scores, w13_mx, w2_mx, out, workspace, dims_FE, 0, MX_STAGES, stream)
+
+
+def moe_fwd_mxfp8_stages(x, topk_ids, topk_scores, w13_mx, w2_mx, out, workspace, dims_FE, stage_begin: int,
+                         stage_end: int, stream=None) -> None:
+    """Stages [stage_begin, stage_end) of the MXFP8 forward (0 dispatch, 1 gate/up, 2 down, 3 combine)."""
     _need(x, "x", torch.bfloat16, 2)
     _need(topk_ids, "topk_ids", torch.int32, 2)
     _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
@@ -385,6 +396,7 @@ def moe_routed_experts_fwd_mxfp8(x, topk_ids, topk_scores, w13_mx, w2_mx, out, w
         if d.numel() < nd or sc.numel() < ns:
             raise ValueError("prepared weight buffers are smaller than moe_mxfp8_weight_bytes")
     sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
-    _check("moe_routed_experts_fwd_mxfp8", load().moe_routed_experts_fwd_mxfp8(
+    _check("moe_fwd_mxfp8_stages", load().moe_fwd_mxfp8_stages(
         _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13_mx[0]), _ptr(w13_mx[1]), _ptr(w2_mx[0]),
-        _ptr(w2_mx[1]), _ptr(out), T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+        _ptr(w2_mx[1]), _ptr(out), T, D, F, E, K, int(stage_begin), int(stage_end), _ptr(workspace),
+        workspace.numel(), _stream_handle(stream)))

@@ -156,7 +156,7 @@ __device__ __forceinline__ PadRowTile decode_pad_row_tile(int32_t tile, const Ge
 }
 
 __device__ __forceinline__ float silu_of(float g, float* sig_out) {
-    const float sig = 1.0f / (1.0f + __expf(-g));
+    const float sig = sigmoid_fast(g);
     *sig_out = sig;
     return g * sig;
 }

@@ -144,6 +144,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Logistic sigmoid and SiLU for the SwiGLU epilogues: exp through the hardware exp2 and the
+// quotient through the reciprocal approximation (__fdividef, 2 ulp). An IEEE-rounded division
+// here made the gate/up epilogue slower than the block-scaled mainloop it overlaps. For g below
+// about -87 the denominator exceeds 2^126 and the result is 0 (the exact value is below 2^-120).
+__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
 __device__ __forceinline__ float pair_score(const GemmArgs& a, int32_t pair) {
     return a.scores_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.scores)[pair])
                          : __ldg(reinterpret_cast<const float*>(a.scores) + pair);

@@ -81,7 +81,7 @@ struct FwdGateUp {
                 for (int j = 0; j < 16; ++j) {
                     const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
                     const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-                    packed[j] = pack_bf16x2(g0 / (1.0f + __expf(-g0)) * u0, g1 / (1.0f + __expf(-g1)) * u1);
+                    packed[j] = pack_bf16x2(silu_fast(g0) * u0, silu_fast(g1) * u1);
                 }
                 store_64B(a.out0 + row * a.F + f0, packed);
             }

@@ -591,10 +591,20 @@ moe_status_t moe_routed_experts_fwd_mxfp8(const void* x, const int32_t* topk_ids
                                           const void* w2_data, const void* w2_scales, void* out, int64_t T,
                                           int32_t D, int32_t F, int32_t E, int32_t K, void* workspace,
                                           size_t workspace_bytes, moe_stream_t stream) {
+    return moe_fwd_mxfp8_stages(x, topk_ids, topk_scores, scores_dtype, w13_data, w13_scales, w2_data, w2_scales, out,
+                                T, D, F, E, K, 0, MOE_MX_STAGES, workspace, workspace_bytes, stream);
+}
+
+moe_status_t moe_fwd_mxfp8_stages(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                  int32_t scores_dtype, const void* w13_data, const void* w13_scales,
+                                  const void* w2_data, const void* w2_scales, void* out, int64_t T, int32_t D,
+                                  int32_t F, int32_t E, int32_t K, int32_t stage_begin, int32_t stage_end,
+                                  void* workspace, size_t workspace_bytes, moe_stream_t stream) {
     moe_status_t st = check_mx_shape(T, D, F, E, K);
     if (st != MOE_OK) return st;
     if (bad_scores_dtype(scores_dtype)) return MOE_ERR_INVALID_ARG;
-    if (T == 0) return MOE_OK;
+    if (stage_begin < 0 || stage_end > MOE_MX_STAGES || stage_begin > stage_end) return MOE_ERR_INVALID_ARG;
+    if (T == 0 || stage_begin == stage_end) return MOE_OK;
     if (!x || !topk_ids || !topk_scores || !w13_data || !w13_scales || !w2_data || !w2_scales || !out || !workspace)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(topk_ids, 4) || !aligned(topk_scores, 4) || !aligned(w13_data, 16) ||
@@ -640,7 +650,7 @@ moe_status_t moe_routed_experts_fwd_mxfp8(const void* x, const int32_t* topk_ids
     p.nblk = L.nblk;
     p.padded_rows = L.padded_rows;
     p.sm_count = dev.sm_count;
-    return launch_mx_forward(p, reinterpret_cast<cudaStream_t>(stream));
+    return launch_mx_forward(p, stage_begin, stage_end, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_get_status(const void* workspace, uint32_t* device_bits, moe_stream_t stream) {

@@ -166,7 +166,9 @@ struct MxProblem {
     int64_t padded_rows;  // capacity of XQ / HQ: 128 * (ceil(R / 128) + min(E, R))
     int sm_count;
 };
-moe_status_t launch_mx_forward(const MxProblem& p, cudaStream_t stream);
+// Stages [stage_begin, stage_end) of: 0 status + routing + gather-quantize, 1 gate/up GEMM,
+// 2 down GEMM, 3 combine.
+moe_status_t launch_mx_forward(const MxProblem& p, int stage_begin, int stage_end, cudaStream_t stream);
 
 // The combine of the route-wise RMSNorm variant: out[t] = sum_k s * y / sqrt(mean(y^2) + eps).
 moe_status_t launch_combine_rmsnorm(const void* y, const int32_t* ids, const void* scores, int32_t scores_dtype,

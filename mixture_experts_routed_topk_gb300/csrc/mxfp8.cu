@@ -222,7 +222,7 @@ struct MxGateUp {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-                    h[j] = gv / (1.0f + __expf(-gv)) * uv;
+                    h[j] = silu_fast(gv) * uv;
                     amax = fmaxf(amax, fabsf(h[j]));
                 }
                 const int e = mx_exponent(amax);
@@ -309,14 +309,15 @@ moe_status_t launch_mx_prepare_weight(int which, const void* w, int32_t D, int32
                : MOE_ERR_CUDA;
 }
 
-moe_status_t launch_mx_forward(const MxProblem& p, cudaStream_t stream) {
-    const int64_t R = p.T * p.K;
-    const int32_t D = p.D, F = p.F, E = p.E;
+namespace {
+
+// Stage 0: status word, routing (the row-tile prefix, with one column tile) and the gather-quantize.
+moe_status_t mx_dispatch(const MxProblem& p, cudaStream_t stream) {
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
     RoutingBuffers b{};
     b.ids = p.ids;
-    b.R = R;
-    b.E = E;
+    b.R = p.T * p.K;
+    b.E = p.E;
     b.nblk = p.nblk;
     b.block_counts = p.block_counts;
     b.block_bases = p.block_bases;
@@ -324,62 +325,83 @@ moe_status_t launch_mx_forward(const MxProblem& p, cudaStream_t stream) {
     b.offsets = p.offsets;
     b.perm = p.perm;
     b.inv = p.inv;
-    b.tiles1 = p.tiles1;  // with one column tile: the row-tile prefix of the padded layout
+    b.tiles1 = p.tiles1;
     b.tiles2 = p.tiles2;
     b.ntiles_n1 = 1;
     b.ntiles_n2 = 1;
     b.status = p.status;
     moe_status_t st = launch_routing(b, stream);
     if (st != MOE_OK) return st;
-    if (launch_pdl(k_mx_gather_quant, dim3(quant_grid(p.padded_rows, p.sm_count)), dim3(256), 0, stream,
-                   static_cast<const uint4*>(p.x), static_cast<const int32_t*>(p.perm),
-                   static_cast<const int32_t*>(p.counts), static_cast<const int32_t*>(p.offsets),
-                   static_cast<const int32_t*>(p.tiles1), E, p.K, D, p.xq, p.xs) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    return launch_pdl(k_mx_gather_quant, dim3(quant_grid(p.padded_rows, p.sm_count)), dim3(256), 0, stream,
+                      static_cast<const uint4*>(p.x), static_cast<const int32_t*>(p.perm),
+                      static_cast<const int32_t*>(p.counts), static_cast<const int32_t*>(p.offsets),
+                      static_cast<const int32_t*>(p.tiles1), p.E, p.K, p.D, p.xq, p.xs) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
 
-    const int64_t nonempty = R < E ? R : E;
-    const int64_t max_row_tiles = ceil_div(R, kBM) + nonempty;
+GemmArgs mx_args(const MxProblem& p) {
     GemmArgs a{};
     a.counts = p.counts;
     a.offsets = p.offsets;
     a.tiles = p.tiles1;
-    a.E = E;
-    a.D = D;
-    a.F = F;
+    a.E = p.E;
+    a.D = p.D;
+    a.F = p.F;
     a.status = p.status;
-    CUtensorMap ta, tb;
+    return a;
+}
 
-    // gate/up + SwiGLU + MX quantization of H
-    if (!make_tmap_u8(&ta, p.xq, D, p.padded_rows, kMxBK, kBM) ||
-        !make_tmap_u8(&tb, p.w13q, D, static_cast<uint64_t>(E) * 2 * F, kMxBK, kMxGateUpF))
+// Upper bound of the row tiles: ceil(R/128) + (experts that can be non-empty).
+int64_t mx_max_row_tiles(const MxProblem& p) {
+    const int64_t R = p.T * p.K;
+    return ceil_div(R, kBM) + (R < p.E ? R : p.E);
+}
+
+// Stage 1: gate/up + SwiGLU + MX quantization of H.
+moe_status_t mx_gate_up(const MxProblem& p, cudaStream_t stream) {
+    GemmArgs a = mx_args(p);
+    CUtensorMap ta, tb;
+    if (!make_tmap_u8(&ta, p.xq, p.D, p.padded_rows, kMxBK, kBM) ||
+        !make_tmap_u8(&tb, p.w13q, p.D, static_cast<uint64_t>(p.E) * 2 * p.F, kMxBK, kMxGateUpF))
         return MOE_ERR_CUDA;
-    a.kblocks = D / kMxBK;
-    a.ntn = static_cast<int32_t>(ceil_div(F, kMxGateUpF));
+    a.kblocks = p.D / kMxBK;
+    a.ntn = static_cast<int32_t>(ceil_div(p.F, kMxGateUpF));
     a.sf_a = p.xs;
     a.sf_b = static_cast<const uint8_t*>(p.w13s);
     a.q_out = p.hq;
     a.sf_out = p.hs;
-    if ((st = launch_gemm<MxGateUp>(ta, tb, a, sm_count_grid(max_row_tiles * a.ntn, p.sm_count), stream)) != MOE_OK)
-        return st;
+    return launch_gemm<MxGateUp>(ta, tb, a, sm_count_grid(mx_max_row_tiles(p) * a.ntn, p.sm_count), stream);
+}
 
-    // down projection + score, rows scattered to pair order
-    if (!make_tmap_u8(&ta, p.hq, F, p.padded_rows, kMxBK, kBM) ||
-        !make_tmap_u8(&tb, p.w2q, F, static_cast<uint64_t>(E) * D, kMxBK, kMxDownN))
+// Stage 2: down projection + score, rows scattered to pair order.
+moe_status_t mx_down(const MxProblem& p, cudaStream_t stream) {
+    GemmArgs a = mx_args(p);
+    CUtensorMap ta, tb;
+    if (!make_tmap_u8(&ta, p.hq, p.F, p.padded_rows, kMxBK, kBM) ||
+        !make_tmap_u8(&tb, p.w2q, p.F, static_cast<uint64_t>(p.E) * p.D, kMxBK, kMxDownN))
         return MOE_ERR_CUDA;
-    a.kblocks = F / kMxBK;
-    a.ntn = static_cast<int32_t>(ceil_div(D, kMxDownN));
+    a.kblocks = p.F / kMxBK;
+    a.ntn = static_cast<int32_t>(ceil_div(p.D, kMxDownN));
     a.sf_a = p.hs;
     a.sf_b = static_cast<const uint8_t*>(p.w2s);
-    a.q_out = nullptr;
-    a.sf_out = nullptr;
     a.perm = p.perm;
     a.scores = p.scores;
     a.scores_bf16 = p.scores_dtype == MOE_SCORES_BF16 ? 1 : 0;
     a.out0 = static_cast<__nv_bfloat16*>(p.y);
-    if ((st = launch_gemm<MxDown>(ta, tb, a, sm_count_grid(max_row_tiles * a.ntn, p.sm_count), stream)) != MOE_OK)
-        return st;
+    return launch_gemm<MxDown>(ta, tb, a, sm_count_grid(mx_max_row_tiles(p) * a.ntn, p.sm_count), stream);
+}
 
-    return launch_combine(p.y, p.ids, p.T, D, E, p.K, p.out, p.sm_count, stream);
+}  // namespace
+
+moe_status_t launch_mx_forward(const MxProblem& p, int stage_begin, int stage_end, cudaStream_t stream) {
+    const auto run = [&](int stage) { return stage_begin <= stage && stage < stage_end; };
+    moe_status_t st = MOE_OK;
+    if (run(0) && (st = mx_dispatch(p, stream)) != MOE_OK) return st;
+    if (run(1) && (st = mx_gate_up(p, stream)) != MOE_OK) return st;
+    if (run(2) && (st = mx_down(p, stream)) != MOE_OK) return st;
+    if (run(3)) st = launch_combine(p.y, p.ids, p.T, p.D, p.E, p.K, p.out, p.sm_count, stream);
+    return st;
 }
 
 }  // namespace moe

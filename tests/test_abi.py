@@ -207,3 +207,15 @@ def test_binding_mx_region_list_matches_header():
     text = open(HEADER).read()
     n = int(re.search(r"MOE_MXWS_REGIONS\s*=\s*(\d+)", text).group(1))
     assert len(binding.MXWS_REGIONS) == n
+
+
+def test_mxfp8_stage_range_validation(lib):
+    v = ctypes.c_void_p
+    st = lambda b, e, **kw: lib.moe_fwd_mxfp8_stages(
+        v(FAKE), v(FAKE), v(FAKE), 0, v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(FAKE), kw.get("T", 16), 256, 256, 8, 2,
+        b, e, v(FAKE), 1 << 40, None)
+    assert st(-1, 2) == INVALID
+    assert st(0, 5) == INVALID
+    assert st(3, 2) == INVALID
+    assert st(2, 2) == OK  # an empty range enqueues nothing
+    assert st(0, 4, T=0) == OK

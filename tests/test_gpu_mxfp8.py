@@ -246,3 +246,14 @@ def test_mxfp8_full_size_sampled_tokens(name, ntok):
     ref, tok = oracle_mx_tokens(d, tokens)
     err = max_rel_err(out.float().cpu().numpy()[tok], ref)
     assert err <= OUT_TOL, err
+
+
+def test_mxfp8_stages_equal_fused_call():
+    T, D, F, E, K = 150, 256, 384, 5, 3
+    d = problem(T, D, F, E, K, seed=9)
+    mx = prepare(d)
+    fused, ws = run_mx(d, mx)
+    out = torch.empty_like(fused)
+    for s in range(binding.MX_STAGES):
+        binding.moe_fwd_mxfp8_stages(d["x"], d["topk_ids"], d["topk_scores"], mx[0], mx[1], out, ws, (F, E), s, s + 1)
+    assert torch.equal(out, fused)

@@ -76,6 +76,15 @@ def load_library(path: str) -> ctypes.CDLL:
         ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
     ]
     lib.oracle_routed_experts_mxfp8.restype = ctypes.c_int
+    lib.oracle_nvfp4_weight_scale.argtypes = [p, ctypes.c_int64]
+    lib.oracle_nvfp4_weight_scale.restype = ctypes.c_float
+    lib.oracle_nvfp4_quantize_rows.argtypes = [p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, p, p]
+    lib.oracle_nvfp4_quantize_rows.restype = ctypes.c_int
+    lib.oracle_routed_experts_nvfp4.argtypes = [
+        p, p, p, ctypes.c_int, p, p, ctypes.c_float, p, p, ctypes.c_float, ctypes.c_float, ctypes.c_float, p,
+        ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+    ]
+    lib.oracle_routed_experts_nvfp4.restype = ctypes.c_int
     return lib
 
 
@@ -272,4 +281,63 @@ def routed_experts_mxfp8(x_bits, topk_ids, topk_scores, w13_mx, w2_mx, nthreads:
     )
     if rc != 0:
         raise RuntimeError("oracle_routed_experts_mxfp8 failed")
+    return out
+
+
+def nvfp4_weight_scale(bits, lib=None) -> float:
+    """The tensor scale G of a bf16 weight: amax / 2688 in fp32 (1 for an all-zero tensor)."""
+    a = np.ascontiguousarray(bits, dtype=np.uint16)
+    return float(_library(lib).oracle_nvfp4_weight_scale(_ptr(a), a.size))
+
+
+def nvfp4_quantize_rows(bits, G: float, lib=None):
+    """NVFP4 quantization of bf16 bits ``[..., cols]`` (cols % 16 == 0) with tensor scale G.
+
+    Returns ``(codes, scales)``: uint8 E2M1 codes (one per byte, low 4 bits) of the same shape and
+    uint8 UE4M3 scale codes ``[..., cols // 16]``.
+    """
+    a = np.ascontiguousarray(bits, dtype=np.uint16)
+    cols = a.shape[-1]
+    rows = a.size // cols if cols else 0
+    codes = np.zeros(a.shape, np.uint8)
+    scales = np.zeros(a.shape[:-1] + (cols // 16,), np.uint8)
+    if _library(lib).oracle_nvfp4_quantize_rows(_ptr(a), rows, cols, float(G), _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError("oracle_nvfp4_quantize_rows rejected its arguments")
+    return codes, scales
+
+
+def nvfp4_prepare(bits, lib=None):
+    """(codes, scales, G) of a bf16 weight with its own tensor scale."""
+    G = nvfp4_weight_scale(bits, lib=lib)
+    codes, scales = nvfp4_quantize_rows(bits, G, lib=lib)
+    return codes, scales, G
+
+
+def routed_experts_nvfp4(x_bits, topk_ids, topk_scores, w13_nv, w2_nv, gx: float, gh: float,
+                         nthreads: int | None = None, lib=None) -> np.ndarray:
+    """out[T,D] (fp32) of the NVFP4 forward. w13_nv = (codes [E,2,F,D], scales [E,2,F,D/16], G),
+    w2_nv = (codes [E,D,F], scales [E,D,F/16], G) from :func:`nvfp4_prepare`; gx and gh are the
+    activation tensor scales of x and of the SwiGLU output."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    w13q, w13s = (np.ascontiguousarray(a, dtype=np.uint8) for a in w13_nv[:2])
+    w2q, w2s = (np.ascontiguousarray(a, dtype=np.uint8) for a in w2_nv[:2])
+    sc = np.asarray(topk_scores)
+    scores_bf16 = 1 if sc.dtype == np.uint16 else 0
+    sc = np.ascontiguousarray(sc, dtype=np.uint16 if scores_bf16 else np.float32)
+    T, D = x.shape
+    E, two, F, D2 = w13q.shape
+    K = ids.shape[1]
+    if (two != 2 or D2 != D or w13s.shape != (E, 2, F, D // 16) or w2q.shape != (E, D, F)
+            or w2s.shape != (E, D, F // 16) or ids.shape[0] != T or sc.shape != ids.shape):
+        raise ValueError("inconsistent shapes")
+    out = np.zeros((T, D), np.float32)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _library(lib).oracle_routed_experts_nvfp4(
+        _ptr(x), _ptr(ids), _ptr(sc), scores_bf16, _ptr(w13q), _ptr(w13s), float(w13_nv[2]), _ptr(w2q), _ptr(w2s),
+        float(w2_nv[2]), float(gx), float(gh), _ptr(out), T, D, F, E, K, int(nthreads),
+    )
+    if rc != 0:
+        raise RuntimeError("oracle_routed_experts_nvfp4 failed")
     return out

@@ -731,3 +731,234 @@ done:
     free(running);
     return rc;
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* NVFP4 forward (inference).                                                                  */
+/*                                                                                             */
+/* Dist-MoE 0.1.0, "Choose a precision and pipeline / NVFP4": the NVFP4 block-scaled format,     */
+/* inference only, with prepared weights. The page names the format, not its encoding; the       */
+/* reading here is NVIDIA's published NVFP4 two-level scaling:                                  */
+/*   - elements E2M1 (sign, 2 exponent bits with bias 1, 1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3,   */
+/*     4, 6), in blocks of 16 consecutive elements along the contraction axis;                  */
+/*   - each block has a scale S: a positive E4M3 value (UE4M3); each tensor has an fp32 scale G; */
+/*   - a block with largest magnitude amax gets S = E4M3(amax / (6 G)) (nearest, ties to even,   */
+/*     saturating at 448); an element v gets E2M1(v / (S G)) (nearest, ties to even, saturating */
+/*     at 6, sign kept), or +0 when S = 0; its value is e2m1 * S * G;                          */
+/*   - the fp32 steps are fixed so that any implementation decides the same codes:              */
+/*     t = 6 G (fp32 product), b = amax / t (fp32 quotient); r = 1 / (S G) as the fp32          */
+/*     reciprocal of the fp32 product S G, and v * r (fp32 product) is rounded to E2M1;         */
+/*   - a weight's G is amax(whole tensor) / 2688 (= 6 * 448) in fp32 (1 for an all-zero tensor); */
+/*     the activations' G (for x and for the SwiGLU output h) are calibration constants given   */
+/*     by the caller, as NVFP4 inference takes its activation scales.                           */
+/* Codes are kept one per byte here (the low 4 bits).                                          */
+
+/* Value of an E2M1 code (4 bits). */
+static double e2m1_value(uint8_t code) {
+    const int sign = (code >> 3) & 1, ex = (code >> 1) & 3, man = code & 1;
+    const double mag = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);
+    return sign ? -mag : mag;
+}
+
+/* The E2M1 code nearest to v: magnitudes 0, 0.5, 1, 1.5 are spaced 0.5, then 2, 3 (spacing 1)
+ * and 4, 6 (spacing 2); ties go to the code with an even mantissa bit; beyond 6 gives 6. */
+static uint8_t e2m1_code(double v) {
+    const uint8_t sign = signbit(v) ? 8 : 0;
+    const double a = fabs(v);
+    double step = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+    /* nearest multiple of the spacing, ties to the even multiple: on this grid an even multiple
+     * is a value with an even mantissa bit (1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4) */
+    double r = nearbyint(a / step) * step;
+    if (r > 6.0) r = 6.0;
+    uint8_t code = 0;
+    for (uint8_t c = 0; c < 8; ++c)
+        if (e2m1_value(c) == r) code = c;
+    return (uint8_t)(sign | code);
+}
+
+/* One block of 16: codes (one per byte) and the block's UE4M3 scale code, for the tensor scale G. */
+static void nvfp4_quantize_block(const float *v, float G, uint8_t *codes, uint8_t *scale_code) {
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i)
+        if (fabsf(v[i]) > amax) amax = fabsf(v[i]);
+    const float t = 6.0f * G;
+    const float b = amax / t;
+    const uint8_t s = (uint8_t)(e4m3_code((double)b) & 0x7F);
+    *scale_code = s;
+    const float S = (float)e4m3_value(s);
+    if (S == 0.0f) {
+        for (int i = 0; i < 16; ++i) codes[i] = 0;
+        return;
+    }
+    const float r = 1.0f / (S * G);
+    for (int i = 0; i < 16; ++i) codes[i] = e2m1_code((double)(v[i] * r));
+}
+
+/* The tensor scale of a weight: amax / 2688 in fp32, 1 for an all-zero tensor. */
+float oracle_nvfp4_weight_scale(const uint16_t *in, int64_t n) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        const float a = fabsf(bf16_to_f32(in[i]));
+        if (a > amax) amax = a;
+    }
+    return amax > 0.0f ? amax / 2688.0f : 1.0f;
+}
+
+/*
+ * NVFP4 quantization of a bf16 matrix [rows, cols] along its rows (cols % 16 == 0) with the
+ * tensor scale G: E2M1 codes [rows, cols] (one per byte) and UE4M3 scale codes [rows, cols / 16].
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_nvfp4_quantize_rows(const uint16_t *in, int64_t rows, int32_t cols, float G, uint8_t *codes,
+                               uint8_t *scales) {
+    if (rows < 0 || cols <= 0 || cols % 16 != 0 || !(G > 0.0f)) return -1;
+    float blk[16];
+    for (int64_t r = 0; r < rows; ++r)
+        for (int32_t b = 0; b < cols / 16; ++b) {
+            for (int i = 0; i < 16; ++i) blk[i] = bf16_to_f32(in[r * cols + b * 16 + i]);
+            nvfp4_quantize_block(blk, G, codes + r * cols + b * 16, scales + r * (cols / 16) + b);
+        }
+    return 0;
+}
+
+/* Dequantized row: e2m1 * S * G, in fp32 (e2m1 * S exact; the product with G rounded once). */
+static void nvfp4_dequantize_row(const uint8_t *codes, const uint8_t *scales, float G, int32_t cols, float *out) {
+    for (int32_t b = 0; b < cols / 16; ++b) {
+        const float S = (float)e4m3_value(scales[b]);
+        for (int i = 0; i < 16; ++i) out[b * 16 + i] = (float)(e2m1_value(codes[b * 16 + i]) * S) * G;
+    }
+}
+
+typedef struct {
+    oracle_job base;
+    const uint8_t *w13q, *w13s, *w2q, *w2s;
+    float g13, g2, gx, gh;
+} oracle_nvfp4_job;
+
+static void *oracle_tokens_nvfp4(void *arg) {
+    oracle_nvfp4_job *nj = (oracle_nvfp4_job *)arg;
+    oracle_job *job = &nj->base;
+    const int32_t D = job->D, F = job->F, E = job->E, K = job->K;
+    float *xt = (float *)malloc(sizeof(float) * (size_t)D);
+    float *xd = (float *)malloc(sizeof(float) * (size_t)D);
+    float *acc = (float *)malloc(sizeof(float) * (size_t)D);
+    float *h = (float *)malloc(sizeof(float) * (size_t)F);
+    float *hd = (float *)malloc(sizeof(float) * (size_t)F);
+    float *wg = (float *)malloc(sizeof(float) * (size_t)D);
+    float *wu = (float *)malloc(sizeof(float) * (size_t)D);
+    float *w2r = (float *)malloc(sizeof(float) * (size_t)F);
+    uint8_t *q = (uint8_t *)malloc((size_t)(D > F ? D : F));
+    uint8_t *qs = (uint8_t *)malloc((size_t)(D > F ? D : F) / 16);
+    if (!xt || !xd || !acc || !h || !hd || !wg || !wu || !w2r || !q || !qs) {
+        job->failed = 1;
+        goto out;
+    }
+    for (int64_t t = job->t_begin; t < job->t_end; ++t) {
+        for (int32_t b = 0; b < D / 16; ++b) {
+            for (int i = 0; i < 16; ++i) xt[b * 16 + i] = bf16_to_f32(job->x[t * D + b * 16 + i]);
+            nvfp4_quantize_block(xt + b * 16, nj->gx, q + b * 16, qs + b);
+        }
+        nvfp4_dequantize_row(q, qs, nj->gx, D, xd);
+        for (int32_t j = 0; j < D; ++j) acc[j] = 0.0f;
+        for (int32_t k = 0; k < K; ++k) {
+            const int32_t e = job->ids[t * K + k];
+            if (e < 0 || e >= E) continue;
+            const float s = pair_score(job, t * K + k);
+            for (int32_t f = 0; f < F; ++f) {
+                const size_t grow = ((size_t)e * 2 + 0) * (size_t)F + (size_t)f;
+                const size_t urow = ((size_t)e * 2 + 1) * (size_t)F + (size_t)f;
+                nvfp4_dequantize_row(nj->w13q + grow * (size_t)D, nj->w13s + grow * (size_t)(D / 16), nj->g13, D, wg);
+                nvfp4_dequantize_row(nj->w13q + urow * (size_t)D, nj->w13s + urow * (size_t)(D / 16), nj->g13, D, wu);
+                float g = 0.0f, u = 0.0f;
+                for (int32_t d = 0; d < D; ++d) {
+                    g += wg[d] * xd[d];
+                    u += wu[d] * xd[d];
+                }
+                h[f] = g / (1.0f + expf(-g)) * u;
+            }
+            for (int32_t b = 0; b < F / 16; ++b) nvfp4_quantize_block(h + b * 16, nj->gh, q + b * 16, qs + b);
+            nvfp4_dequantize_row(q, qs, nj->gh, F, hd);
+            for (int32_t j = 0; j < D; ++j) {
+                const size_t row = (size_t)e * (size_t)D + (size_t)j;
+                nvfp4_dequantize_row(nj->w2q + row * (size_t)F, nj->w2s + row * (size_t)(F / 16), nj->g2, F, w2r);
+                float y = 0.0f;
+                for (int32_t f = 0; f < F; ++f) y += w2r[f] * hd[f];
+                acc[j] += s * y;
+            }
+        }
+        for (int32_t j = 0; j < D; ++j) job->out[t * D + j] = acc[j];
+    }
+out:
+    free(xt);
+    free(xd);
+    free(acc);
+    free(h);
+    free(hd);
+    free(wg);
+    free(wu);
+    free(w2r);
+    free(q);
+    free(qs);
+    return NULL;
+}
+
+/*
+ * out[T,D] (fp32) of the NVFP4 forward. x [T,D] bf16 bits, quantized per token row with the
+ * activation scale gx; the SwiGLU output h is quantized per pair with gh; the weights prepared by
+ * oracle_nvfp4_quantize_rows: w13q [E,2F,D] codes, w13s [E,2F,D/16] scale codes, tensor scale g13;
+ * w2q [E,D,F], w2s [E,D,F/16], g2. D and F multiples of 16. ids, scores as for
+ * oracle_routed_experts. Returns 0, or -1 on a bad argument or an allocation failure.
+ */
+int oracle_routed_experts_nvfp4(const uint16_t *x, const int32_t *ids, const void *scores, int scores_bf16,
+                                const uint8_t *w13q, const uint8_t *w13s, float g13, const uint8_t *w2q,
+                                const uint8_t *w2s, float g2, float gx, float gh, float *out, int64_t T, int32_t D,
+                                int32_t F, int32_t E, int32_t K, int nthreads) {
+    if (T < 0 || D <= 0 || F <= 0 || E <= 0 || K <= 0 || D % 16 != 0 || F % 16 != 0) return -1;
+    if (!(g13 > 0.0f) || !(g2 > 0.0f) || !(gx > 0.0f) || !(gh > 0.0f)) return -1;
+    if (T == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > T) nthreads = (int)T;
+    oracle_nvfp4_job *jobs = (oracle_nvfp4_job *)calloc((size_t)nthreads, sizeof(oracle_nvfp4_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    unsigned char *running = (unsigned char *)calloc((size_t)nthreads, 1);
+    int rc = 0;
+    if (!jobs || !tids || !running) {
+        rc = -1;
+        goto done;
+    }
+    for (int i = 0; i < nthreads; ++i) {
+        oracle_nvfp4_job *j = &jobs[i];
+        j->base.x = x;
+        j->base.ids = ids;
+        j->base.scores = scores;
+        j->base.scores_bf16 = scores_bf16;
+        j->base.out = out;
+        j->base.t_begin = T * i / nthreads;
+        j->base.t_end = T * (i + 1) / nthreads;
+        j->base.D = D;
+        j->base.F = F;
+        j->base.E = E;
+        j->base.K = K;
+        j->w13q = w13q;
+        j->w13s = w13s;
+        j->w2q = w2q;
+        j->w2s = w2s;
+        j->g13 = g13;
+        j->g2 = g2;
+        j->gx = gx;
+        j->gh = gh;
+    }
+    for (int i = 1; i < nthreads; ++i)
+        running[i] = (pthread_create(&tids[i], NULL, oracle_tokens_nvfp4, &jobs[i]) == 0);
+    oracle_tokens_nvfp4(&jobs[0]);
+    for (int i = 1; i < nthreads; ++i)
+        if (running[i]) pthread_join(tids[i], NULL);
+    for (int i = 1; i < nthreads; ++i)
+        if (!running[i]) oracle_tokens_nvfp4(&jobs[i]);
+    for (int i = 0; i < nthreads; ++i)
+        if (jobs[i].base.failed) rc = -1;
+done:
+    free(jobs);
+    free(tids);
+    free(running);
+    return rc;
+}

@@ -11,6 +11,7 @@ import pytest
 import oracle
 import oracle_bwd_pins
 import oracle_mx_pins
+import oracle_nvfp4_pins
 import oracle_pins
 
 MUTANTS = {
@@ -63,6 +64,18 @@ MUTANTS = {
     "mx_x_not_quantized": [("g += wg[d] * xd[d];\n                    u += wu[d] * xd[d];",
                             "g += wg[d] * xt[d];\n                    u += wu[d] * xt[d];")],
     "mx_gate_uses_up_scales": [("job->w13s + grow * (size_t)(D / 32)", "job->w13s + urow * (size_t)(D / 32)")],
+    # NVFP4: the two-level format and the block-scaled forward
+    "nv_scale_over_4": [("const float t = 6.0f * G;", "const float t = 4.0f * G;")],
+    "nv_ties_away_from_zero": [("double r = nearbyint(a / step) * step;", "double r = round(a / step) * step;")],
+    "nv_no_saturation": [("if (r > 6.0) r = 6.0;", "")],
+    "nv_zero_scale_unguarded": [("    if (S == 0.0f) {\n        for (int i = 0; i < 16; ++i) codes[i] = 0;\n        return;\n    }\n", "")],
+    "nv_tensor_scale_not_applied": [("out[b * 16 + i] = (float)(e2m1_value(codes[b * 16 + i]) * S) * G;",
+                                     "out[b * 16 + i] = (float)(e2m1_value(codes[b * 16 + i]) * S);")],
+    "nv_weight_scale_448": [("return amax > 0.0f ? amax / 2688.0f : 1.0f;", "return amax > 0.0f ? amax / 448.0f : 1.0f;")],
+    "nv_h_not_quantized": [("nvfp4_dequantize_row(q, qs, nj->gh, F, hd);", "memcpy(hd, h, sizeof(float) * (size_t)F);")],
+    "nv_x_scale_dropped": [("nvfp4_dequantize_row(q, qs, nj->gx, D, xd);", "nvfp4_dequantize_row(q, qs, 1.0f, D, xd);")],
+    "nv_scales_per_32": [("const float S = (float)e4m3_value(scales[b]);", "const float S = (float)e4m3_value(scales[b / 2]);")],
+    "nv_sign_lost": [("const uint8_t sign = signbit(v) ? 8 : 0;", "const uint8_t sign = 0;")],
 }
 
 
@@ -79,7 +92,7 @@ def test_pins_reject_mutant(name, tmp_path):
     oracle.compile_oracle(str(path), lib_path)
     lib = oracle.load_library(lib_path)
     failed = []
-    for check in oracle_pins.ALL_PINS + oracle_bwd_pins.BWD_PINS + oracle_mx_pins.MX_PINS:
+    for check in oracle_pins.ALL_PINS + oracle_bwd_pins.BWD_PINS + oracle_mx_pins.MX_PINS + oracle_nvfp4_pins.NV_PINS:
         try:
             check(lib=lib)
         except AssertionError:

@@ -351,6 +351,78 @@ moe_status_t moe_fwd_mxfp8_stages(const void *x, const int32_t *topk_ids, const 
                                   int32_t F, int32_t E, int32_t K, int32_t stage_begin, int32_t stage_end,
                                   void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------ */
+/* NVFP4 forward, inference (Dist-MoE 0.1.0, "Choose a precision and pipeline / NVFP4":          */
+/* inference only, prepared weights).                                                          */
+/*                                                                                              */
+/* The format, read as NVIDIA's two-level NVFP4: E2M1 elements in blocks of 16 along a GEMM's    */
+/* contraction axis; a block scale S = E4M3(amax / (6 G)) stored as a UE4M3 byte (nearest even, */
+/* saturating at 448); a per-tensor fp32 scale G; elements E2M1(v / (S G)) (nearest even,       */
+/* saturating at 6, sign kept; +0 when S = 0), value = e2m1 * S * G. The fp32 steps are fixed:   */
+/* t = 6 G, b = amax / t, r = 1 / (S G) (IEEE reciprocal of the fp32 product), v * r. A weight's */
+/* G = amax(tensor) / 2688, found by moe_nvfp4_prepare_weight; the activations' G (x_scale for x, */
+/* h_scale for the SwiGLU output) are calibration constants passed to the forward call. E2M1    */
+/* codes are packed two per byte, the lower K index in the low nibble.                          */
+/* Shape limits: those of the MXFP8 entry points (D and F multiples of 128).                    */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * Sizes of a prepared NVFP4 weight (host outputs, caller-owned). Pure arithmetic.
+ *   MOE_WEIGHT_W13: data E*2F*D/2;  scales 256 + E * ceil(F/64) * P(D) * 512
+ *   MOE_WEIGHT_W2:  data E*D*F/2;   scales 256 + E * ceil(D/128) * P(F) * 512
+ * with P(C) = 4 * ceil(C/256) scale groups of 64 K values per row (padded to whole 256-wide steps).
+ */
+moe_status_t moe_nvfp4_weight_bytes(int32_t which, int32_t D, int32_t F, int32_t E, size_t *data_bytes,
+                                    size_t *scale_bytes);
+
+/*
+ * Prepares one expert weight for the NVFP4 forward:
+ *   w       device bf16: w13 [E,2,F,D] (MOE_WEIGHT_W13) or w2 [E,D,F] (MOE_WEIGHT_W2)
+ *   data    device: packed E2M1 codes in w's element order (w13 as [E*2F, D/2] bytes, w2 as
+ *           [E*D, F/2])
+ *   scales  device, 256-byte aligned: a 256-byte header (the fp32 tensor scale G at byte 0), then
+ *           the UE4M3 scales grouped per GEMM tile: the scale of row n of tile (e, j) and 16-block
+ *           b along the row sits at byte
+ *             256 + ((e * NT + j) * P(C) + b / 4) * 512 + 16 * (n % 32) + 4 * (n / 32) + b % 4
+ *           with C the row length. w13: NT = ceil(F/64), tile j holds gate rows f = 64j + n (n < 64)
+ *           then up rows f = 64j + n - 64; w2: NT = ceil(D/128), row d = 128j + n. Bytes that belong
+ *           to no row are 0.
+ * Deterministic. Capacities at least moe_nvfp4_weight_bytes' (MOE_ERR_WORKSPACE_TOO_SMALL otherwise).
+ */
+moe_status_t moe_nvfp4_prepare_weight(int32_t which, const void *w, int32_t D, int32_t F, int32_t E,
+                                      void *data, size_t data_bytes, void *scales, size_t scale_bytes,
+                                      moe_stream_t stream);
+
+/* Bytes of device workspace of the NVFP4 forward, and its layout: the MOE_MXWS_* regions, with XQ
+ * and HQ holding packed E2M1 codes ([Rp, D/2] and [Rp, F/2] bytes) and XS and HS UE4M3 scales
+ * (padded row p, 16-block b at byte ((p/128) * P(cols) + b/4) * 512 + 16 (p%32) + 4 ((p%128)/32)
+ * + b%4). Pure arithmetic. */
+size_t moe_nvfp4_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K);
+moe_status_t moe_nvfp4_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                        size_t *region_offsets);
+
+/*
+ * The NVFP4 forward: out as for moe_routed_experts_fwd, computed from NVFP4-quantized x (tensor
+ * scale x_scale), w13, h (tensor scale h_scale) and w2, with fp32 accumulation (block-scaled
+ * tcgen05 tensor-core GEMMs). x_scale and h_scale: finite and > 0 (MOE_ERR_INVALID_ARG otherwise).
+ * Other arguments as for moe_routed_experts_fwd_mxfp8, with weights from
+ * moe_nvfp4_prepare_weight and a workspace of moe_nvfp4_workspace_bytes.
+ */
+moe_status_t moe_routed_experts_fwd_nvfp4(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                          int32_t scores_dtype, const void *w13_data, const void *w13_scales,
+                                          const void *w2_data, const void *w2_scales, float x_scale,
+                                          float h_scale, void *out, int64_t T, int32_t D, int32_t F, int32_t E,
+                                          int32_t K, void *workspace, size_t workspace_bytes,
+                                          moe_stream_t stream);
+
+/* Stages stage_begin .. stage_end-1 (MOE_MX_STAGE_*) of moe_routed_experts_fwd_nvfp4. */
+moe_status_t moe_fwd_nvfp4_stages(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                  int32_t scores_dtype, const void *w13_data, const void *w13_scales,
+                                  const void *w2_data, const void *w2_scales, float x_scale, float h_scale,
+                                  void *out, int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                  int32_t stage_begin, int32_t stage_end, void *workspace,
+                                  size_t workspace_bytes, moe_stream_t stream);
+
 /* Capacity of the library-owned scratch of moe_routing_static_scratch, in int32 entries per
  * array: it serves sizes with (E + 1) * ceil(T*K / 2048) <= this value. */
 #define MOE_STATIC_SCRATCH_MAX_ENTRIES 262144

@@ -24,6 +24,12 @@ __all__ = [
     "moe_mxfp8_workspace_layout",
     "moe_routed_experts_fwd_mxfp8",
     "moe_fwd_mxfp8_stages",
+    "moe_nvfp4_weight_bytes",
+    "moe_nvfp4_prepare_weight",
+    "moe_nvfp4_workspace_bytes",
+    "moe_nvfp4_workspace_layout",
+    "moe_routed_experts_fwd_nvfp4",
+    "moe_fwd_nvfp4_stages",
     "MOE_WEIGHT_W13",
     "MOE_WEIGHT_W2",
     "moe_get_status",

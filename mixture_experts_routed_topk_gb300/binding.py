@@ -87,6 +87,16 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "moe_mxfp8_workspace_layout": ([i64, i32, i32, i32, i32, vp], ctypes.c_int),
             "moe_routed_experts_fwd_mxfp8": (
                 [vp, vp, vp, i32, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_nvfp4_weight_bytes": ([i32, i32, i32, i32, vp, vp], ctypes.c_int),
+            "moe_nvfp4_prepare_weight": ([i32, vp, i32, i32, i32, vp, sz, vp, sz, vp], ctypes.c_int),
+            "moe_nvfp4_workspace_bytes": ([i64, i32, i32, i32, i32], sz),
+            "moe_nvfp4_workspace_layout": ([i64, i32, i32, i32, i32, vp], ctypes.c_int),
+            "moe_fwd_nvfp4_stages": (
+                [vp, vp, vp, i32, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, i64, i32, i32, i32, i32, i32,
+                 i32, vp, sz, vp], ctypes.c_int),
+            "moe_routed_experts_fwd_nvfp4": (
+                [vp, vp, vp, i32, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, i64, i32, i32, i32, i32, vp, sz,
+                 vp], ctypes.c_int),
             "moe_fwd_mxfp8_stages": (
                 [vp, vp, vp, i32, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
         }
@@ -400,3 +410,85 @@ def moe_fwd_mxfp8_stages(x, topk_ids, topk_scores, w13_mx, w2_mx, out, workspace
         _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13_mx[0]), _ptr(w13_mx[1]), _ptr(w2_mx[0]),
         _ptr(w2_mx[1]), _ptr(out), T, D, F, E, K, int(stage_begin), int(stage_end), _ptr(workspace),
         workspace.numel(), _stream_handle(stream)))
+
+
+# ------------------------------------------------------------------------------------- NVFP4
+
+def moe_nvfp4_weight_bytes(which: int, D: int, F: int, E: int) -> tuple[int, int]:
+    """(data bytes, scale bytes) of a prepared NVFP4 weight (which = MOE_WEIGHT_W13 or _W2)."""
+    data, scales = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("moe_nvfp4_weight_bytes", load().moe_nvfp4_weight_bytes(
+        int(which), D, F, E, ctypes.byref(data), ctypes.byref(scales)))
+    return int(data.value), int(scales.value)
+
+
+def moe_nvfp4_prepare_weight(which: int, w, data=None, scales=None, stream=None):
+    """Quantizes w13 [E,2,F,D] or w2 [E,D,F] to NVFP4. Returns (data, scales) uint8 device tensors:
+    packed E2M1 codes, and a 256-byte header holding the tensor scale followed by the UE4M3 scales."""
+    _need(w, "w", torch.bfloat16)
+    if which == MOE_WEIGHT_W13:
+        if w.dim() != 4 or w.shape[1] != 2:
+            raise ValueError(f"w13 must be [E,2,F,D], got {tuple(w.shape)}")
+        E, _, F, D = w.shape
+    elif which == MOE_WEIGHT_W2:
+        if w.dim() != 3:
+            raise ValueError(f"w2 must be [E,D,F], got {tuple(w.shape)}")
+        E, D, F = w.shape
+    else:
+        raise ValueError("which must be MOE_WEIGHT_W13 or MOE_WEIGHT_W2")
+    nd, ns = moe_nvfp4_weight_bytes(which, D, F, E)
+    if data is None:
+        data = torch.empty(nd, dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty(ns, dtype=torch.uint8, device=w.device)
+    _need(data, "data", torch.uint8)
+    _need(scales, "scales", torch.uint8)
+    _check("moe_nvfp4_prepare_weight", load().moe_nvfp4_prepare_weight(
+        int(which), _ptr(w), D, F, E, _ptr(data), data.numel(), _ptr(scales), scales.numel(), _stream_handle(stream)))
+    return data, scales
+
+
+def moe_nvfp4_workspace_bytes(T: int, D: int, F: int, E: int, K: int) -> int:
+    return int(load().moe_nvfp4_workspace_bytes(T, D, F, E, K))
+
+
+def moe_nvfp4_workspace_layout(T: int, D: int, F: int, E: int, K: int) -> dict:
+    arr = (ctypes.c_size_t * len(MXWS_REGIONS))()
+    _check("moe_nvfp4_workspace_layout",
+           load().moe_nvfp4_workspace_layout(T, D, F, E, K, ctypes.cast(arr, ctypes.c_void_p)))
+    return dict(zip(MXWS_REGIONS, (int(v) for v in arr)))
+
+
+def moe_routed_experts_fwd_nvfp4(x, topk_ids, topk_scores, w13_nv, w2_nv, out, workspace, dims_FE, x_scale: float,
+                                 h_scale: float, stream=None) -> None:
+    """The NVFP4 forward. w13_nv, w2_nv: (data, scales) from moe_nvfp4_prepare_weight; dims_FE = (F, E);
+    x_scale, h_scale: the activations' tensor scales (calibration constants)."""
+    moe_fwd_nvfp4_stages(x, topk_ids, topk_scores, w13_nv, w2_nv, out, workspace, dims_FE, x_scale, h_scale, 0,
+                         MX_STAGES, stream)
+
+
+def moe_fwd_nvfp4_stages(x, topk_ids, topk_scores, w13_nv, w2_nv, out, workspace, dims_FE, x_scale: float,
+                         h_scale: float, stage_begin: int, stage_end: int, stream=None) -> None:
+    """Stages [stage_begin, stage_end) of the NVFP4 forward (0 dispatch, 1 gate/up, 2 down, 3 combine)."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
+    _need(out, "out", torch.bfloat16, 2)
+    _need(workspace, "workspace", torch.uint8)
+    for name, t in (("w13 data", w13_nv[0]), ("w13 scales", w13_nv[1]), ("w2 data", w2_nv[0]),
+                    ("w2 scales", w2_nv[1])):
+        _need(t, name, torch.uint8)
+    T, D = x.shape
+    K = topk_ids.shape[1]
+    F, E = (int(v) for v in dims_FE)
+    if tuple(out.shape) != (T, D) or tuple(topk_scores.shape) != (T, K) or topk_ids.shape[0] != T:
+        raise ValueError("inconsistent shapes among x [T,D], topk_ids/topk_scores [T,K], out [T,D]")
+    for which, (d, sc) in ((MOE_WEIGHT_W13, w13_nv), (MOE_WEIGHT_W2, w2_nv)):
+        nd, ns = moe_nvfp4_weight_bytes(which, D, F, E)
+        if d.numel() < nd or sc.numel() < ns:
+            raise ValueError("prepared weight buffers are smaller than moe_nvfp4_weight_bytes")
+    sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
+    _check("moe_fwd_nvfp4_stages", load().moe_fwd_nvfp4_stages(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13_nv[0]), _ptr(w13_nv[1]), _ptr(w2_nv[0]),
+        _ptr(w2_nv[1]), float(x_scale), float(h_scale), _ptr(out), T, D, F, E, K, int(stage_begin),
+        int(stage_end), _ptr(workspace), workspace.numel(), _stream_handle(stream)))

@@ -10,6 +10,9 @@
 //
 // The policy's Shape fixes the ring and the MMA kind (Bf16Shape unless the policy names another):
 //   Bf16Shape: 4 stages of 16 KB A + 32 KB B (64 bf16 of K), 128 x 256 accumulators, kind::f16.
+//   Nvf4Shape: 5 stages of 16 KB A + 16 KB B (256 packed E2M1 of K) + 4 KB of UE4M3 scale chunks,
+//              128 x 128 accumulators, kind::mxf4nvf4 block-scaled (four scale chunks per operand
+//              per stage, one per K=64 MMA).
 //   Mxf8Shape: 4 stages of 16 KB A + 24 KB B (128 E4M3 of K) + their UE8M0 scale chunks (512 B
 //              for A's 128 rows, 1 KB for B's 192 rows), 128 x 192 accumulators (TMEM columns
 //              0..191 and 256..447), kind::mxf8f6f4 block-scaled; the MMA thread copies a stage's
@@ -74,7 +77,36 @@ struct Mxf8Shape {
     // Scale slot of stage s (32 columns: A's scales at +0, B's at +16): in the two gaps after the
     // accumulators, columns 192..255 and 448..511.
     __device__ static constexpr uint32_t sf_slot_col(uint32_t s) { return (s & 2u) * 128u + 192u + 32u * (s & 1u); }
+    // One A chunk (128 rows x 4 blocks of 32 = the stage's K) read by all four MMAs through the
+    // scale-factor id; two B chunks (192 rows).
+    static constexpr int kSfaChunks = 1, kSfbChunks = 2;
+    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t slot, int kk,
+                               uint32_t acc) {
+        mma_mxf8_ss(d, a, b, idesc | mxf8_ids(kk), slot, slot + 16u, acc);
+    }
 };
+
+// Packed E2M1 operands with UE4M3 scales per 16: 256 K elements (128 bytes) per stage, four K=64
+// MMAs, each with its own A and B scale chunk. 128 x 128 accumulators at TMEM columns 0 and 256;
+// 32-column scale slots at 128, 160, 192, 224 and 384 (A's four chunks at +0..+12, B's at +16..+28).
+constexpr int kNvBN = 128;
+struct Nvf4Shape {
+    static constexpr int kStages = 5;
+    static constexpr int kABytes = kBM * 128;           // 16 KB
+    static constexpr int kBBytes = kNvBN * 128;         // 16 KB
+    static constexpr int kSfaBytes = 2048, kSfbBytes = 2048;
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 36 KB
+    static constexpr int kTxBytes = kStageBytes;
+    static constexpr int kAccCols = 256;
+    static constexpr bool kBlockScaled = true;
+    __device__ static constexpr uint32_t sf_slot_col(uint32_t s) { return s < 4u ? 128u + 32u * s : 384u; }
+    static constexpr int kSfaChunks = 4, kSfbChunks = 4;
+    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t slot, int kk,
+                               uint32_t acc) {
+        mma_nvf4_ss(d, a, b, idesc, slot + 4u * kk, slot + 16u + 4u * kk, acc);
+    }
+};
+static_assert(Nvf4Shape::kStageBytes % 1024 == 0 && Nvf4Shape::kStages == 5, "stage ring / scale slots");
 static_assert(Mxf8Shape::kStageBytes % 1024 == 0 && Mxf8Shape::kTxBytes <= Mxf8Shape::kStageBytes, "stage");
 static_assert(Mxf8Shape::kStages == 4 && kMxBN + 64 == Mxf8Shape::kAccCols, "four 32-column scale slots in the gaps");
 
@@ -109,7 +141,9 @@ template <class S>
 constexpr size_t gemm_smem_bytes() {
     return 1024 + static_cast<size_t>(S::kStages) * S::kStageBytes + kEpilogueStagingBytes + sizeof(PipeState);
 }
-static_assert(gemm_smem_bytes<Mxf8Shape>() <= 232448 && gemm_smem_bytes<Bf16Shape>() <= 232448, "smem");
+static_assert(gemm_smem_bytes<Mxf8Shape>() <= 232448 && gemm_smem_bytes<Bf16Shape>() <= 232448 &&
+                  gemm_smem_bytes<Nvf4Shape>() <= 232448,
+              "smem");
 
 // Everything any policy needs (each policy reads its own fields).
 struct GemmArgs {
@@ -137,6 +171,8 @@ struct GemmArgs {
     uint8_t* q_out;          // E4M3 output codes
     uint8_t* sf_out;         // the output's scale chunks
     int32_t ntn;             // column tiles per row tile
+    float act_scale_a;       // NVFP4: tensor scale of the A operand's activations
+    float act_scale_out;     // NVFP4: tensor scale used to quantize the epilogue's output
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -321,16 +357,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if constexpr (S::kBlockScaled) {
                         // this stage's scales into its TMEM slot; the slot's previous reader (the MMAs
                         // of stage use it - kStages) completed before the stage was refilled
-                        const uint32_t sf0 = b0 + S::kBBytes;
-                        const uint32_t sfa_t = tmem_base + S::sf_slot_col(s);
-                        const uint32_t sfb_t = sfa_t + 16u;
-                        tmem_cp_scale_chunk(sfa_t, sf_chunk_desc(sf0));
-                        tmem_cp_scale_chunk(sfb_t, sf_chunk_desc(sf0 + 512));
-                        tmem_cp_scale_chunk(sfb_t + 4u, sf_chunk_desc(sf0 + 1024));
+                        const uint32_t sf0 = b0 + S::kBBytes;  // A's chunks, then B's, 512 bytes each
+                        const uint32_t slot = tmem_base + S::sf_slot_col(s);
 #pragma unroll
-                        for (int kk = 0; kk < kMxBK / 32; ++kk)
-                            mma_mxf8_ss(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
-                                        P::kIdesc | mxf8_ids(kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+                        for (int c = 0; c < S::kSfaChunks; ++c)
+                            tmem_cp_scale_chunk(slot + 4u * c, sf_chunk_desc(sf0 + 512 * c));
+#pragma unroll
+                        for (int c = 0; c < S::kSfbChunks; ++c)
+                            tmem_cp_scale_chunk(slot + 16u + 4u * c, sf_chunk_desc(sf0 + S::kSfaBytes + 512 * c));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)  // 128-byte stage rows, 32 bytes of K per MMA
+                            S::mma(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
+                                   P::kIdesc, slot, kk, (kb | kk) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)

@@ -269,7 +269,9 @@ struct MxLayout {
     int64_t padded_rows;
 };
 
-bool make_mx_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, MxLayout* L) {
+// fp4 = true: the NVFP4 sizes (packed E2M1 codes, one UE4M3 scale per 16, K groups padded to whole
+// 256-wide stages); false: MXFP8 (E4M3 codes, one UE8M0 scale per 32).
+bool make_mx_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, MxLayout* L, bool fp4 = false) {
     if (check_mx_shape(T, D, F, E, K) != MOE_OK || T == 0) return false;
     const int64_t R = T * static_cast<int64_t>(K);
     const int64_t nonempty = R < E ? R : E;
@@ -286,10 +288,10 @@ bool make_mx_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, MxLay
     sizes[MOE_MXWS_BLOCK_BASES] = sizeof(int32_t) * e1 * L->nblk;
     sizes[MOE_MXWS_PERM] = sizeof(int32_t) * R;
     sizes[MOE_MXWS_INV] = sizeof(int32_t) * R;
-    sizes[MOE_MXWS_XQ] = rp * D;
-    sizes[MOE_MXWS_XS] = rp * (D / 32);
-    sizes[MOE_MXWS_HQ] = rp * F;
-    sizes[MOE_MXWS_HS] = rp * (F / 32);
+    sizes[MOE_MXWS_XQ] = fp4 ? rp * D / 2 : rp * D;
+    sizes[MOE_MXWS_XS] = fp4 ? nv_act_scale_bytes(L->padded_rows, D) : rp * (D / 32);
+    sizes[MOE_MXWS_HQ] = fp4 ? rp * F / 2 : rp * F;
+    sizes[MOE_MXWS_HS] = fp4 ? nv_act_scale_bytes(L->padded_rows, F) : rp * (F / 32);
     sizes[MOE_MXWS_Y] = 2 * static_cast<size_t>(R) * D;
     size_t off = 0;
     for (int r = 0; r < MOE_MXWS_TOTAL; ++r) {
@@ -309,6 +311,71 @@ bool mx_weight_bytes(int32_t which, int32_t D, int32_t F, int32_t E, size_t* dat
         *scales = static_cast<size_t>(E) * ceil_div(D, kMxDownN) * (F / 128) * 1024;
     }
     return true;
+}
+
+
+// The block-scaled forward stages (MXFP8, or NVFP4 with fp4 = true and its activation scales).
+moe_status_t block_scaled_stages(bool fp4, const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                 int32_t scores_dtype, const void* w13_data, const void* w13_scales,
+                                 const void* w2_data, const void* w2_scales, float x_scale, float h_scale, void* out,
+                                 int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, int32_t stage_begin,
+                                 int32_t stage_end, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    moe_status_t st = check_mx_shape(T, D, F, E, K);
+    if (fp4 && !(x_scale > 0.0f && x_scale < 3.0e38f && h_scale > 0.0f && h_scale < 3.0e38f))
+        return MOE_ERR_INVALID_ARG;
+    if (st != MOE_OK) return st;
+    if (bad_scores_dtype(scores_dtype)) return MOE_ERR_INVALID_ARG;
+    if (stage_begin < 0 || stage_end > MOE_MX_STAGES || stage_begin > stage_end) return MOE_ERR_INVALID_ARG;
+    if (T == 0 || stage_begin == stage_end) return MOE_OK;
+    if (!x || !topk_ids || !topk_scores || !w13_data || !w13_scales || !w2_data || !w2_scales || !out || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(topk_ids, 4) || !aligned(topk_scores, 4) || !aligned(w13_data, 16) ||
+        !aligned(w13_scales, 256) || !aligned(w2_data, 16) || !aligned(w2_scales, 256) || !aligned(out, 16) ||
+        !aligned(workspace, kAlign))
+        return MOE_ERR_MISALIGNED;
+    MxLayout L;
+    if (!make_mx_layout(T, D, F, E, K, &L, fp4)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (workspace_bytes < L.off[MOE_MXWS_TOTAL]) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != MOE_OK) return st;
+    if (!dev.supported) return MOE_ERR_UNSUPPORTED_DEVICE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    MxProblem p{};
+    p.act_scale_x = x_scale;
+    p.act_scale_h = h_scale;
+    p.T = T;
+    p.D = D;
+    p.F = F;
+    p.E = E;
+    p.K = K;
+    p.x = x;
+    p.ids = topk_ids;
+    p.scores = topk_scores;
+    p.scores_dtype = scores_dtype;
+    p.w13q = w13_data;
+    p.w13s = w13_scales;
+    p.w2q = w2_data;
+    p.w2s = w2_scales;
+    p.out = out;
+    p.status = reinterpret_cast<uint32_t*>(ws + L.off[MOE_MXWS_STATUS]);
+    p.counts = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_COUNTS]);
+    p.offsets = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_OFFSETS]);
+    p.tiles1 = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_TILES]);
+    p.tiles2 = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_TILES2]);
+    p.block_counts = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_BLOCK_COUNTS]);
+    p.block_bases = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_BLOCK_BASES]);
+    p.perm = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_PERM]);
+    p.inv = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_INV]);
+    p.xq = ws + L.off[MOE_MXWS_XQ];
+    p.xs = ws + L.off[MOE_MXWS_XS];
+    p.hq = ws + L.off[MOE_MXWS_HQ];
+    p.hs = ws + L.off[MOE_MXWS_HS];
+    p.y = ws + L.off[MOE_MXWS_Y];
+    p.nblk = L.nblk;
+    p.padded_rows = L.padded_rows;
+    p.sm_count = dev.sm_count;
+    return fp4 ? launch_nv_forward(p, stage_begin, stage_end, reinterpret_cast<cudaStream_t>(stream))
+               : launch_mx_forward(p, stage_begin, stage_end, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -595,62 +662,78 @@ moe_status_t moe_routed_experts_fwd_mxfp8(const void* x, const int32_t* topk_ids
                                 T, D, F, E, K, 0, MOE_MX_STAGES, workspace, workspace_bytes, stream);
 }
 
+
 moe_status_t moe_fwd_mxfp8_stages(const void* x, const int32_t* topk_ids, const void* topk_scores,
                                   int32_t scores_dtype, const void* w13_data, const void* w13_scales,
                                   const void* w2_data, const void* w2_scales, void* out, int64_t T, int32_t D,
                                   int32_t F, int32_t E, int32_t K, int32_t stage_begin, int32_t stage_end,
                                   void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-    moe_status_t st = check_mx_shape(T, D, F, E, K);
+    return block_scaled_stages(false, x, topk_ids, topk_scores, scores_dtype, w13_data, w13_scales, w2_data,
+                               w2_scales, 0.0f, 0.0f, out, T, D, F, E, K, stage_begin, stage_end, workspace,
+                               workspace_bytes, stream);
+}
+
+moe_status_t moe_nvfp4_weight_bytes(int32_t which, int32_t D, int32_t F, int32_t E, size_t* data_bytes,
+                                    size_t* scale_bytes) {
+    if (!data_bytes || !scale_bytes) return MOE_ERR_INVALID_ARG;
+    if (which != MOE_WEIGHT_W13 && which != MOE_WEIGHT_W2) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_mx_shape(1, D, F, E, 1);
     if (st != MOE_OK) return st;
-    if (bad_scores_dtype(scores_dtype)) return MOE_ERR_INVALID_ARG;
-    if (stage_begin < 0 || stage_end > MOE_MX_STAGES || stage_begin > stage_end) return MOE_ERR_INVALID_ARG;
-    if (T == 0 || stage_begin == stage_end) return MOE_OK;
-    if (!x || !topk_ids || !topk_scores || !w13_data || !w13_scales || !w2_data || !w2_scales || !out || !workspace)
-        return MOE_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(topk_ids, 4) || !aligned(topk_scores, 4) || !aligned(w13_data, 16) ||
-        !aligned(w13_scales, 256) || !aligned(w2_data, 16) || !aligned(w2_scales, 256) || !aligned(out, 16) ||
-        !aligned(workspace, kAlign))
-        return MOE_ERR_MISALIGNED;
-    MxLayout L;
-    if (!make_mx_layout(T, D, F, E, K, &L)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (workspace_bytes < L.off[MOE_MXWS_TOTAL]) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    *data_bytes = (which == MOE_WEIGHT_W13 ? static_cast<size_t>(E) * 2 * F * D : static_cast<size_t>(E) * D * F) / 2;
+    *scale_bytes = nv_weight_scale_bytes(which, D, F, E);
+    return MOE_OK;
+}
+
+moe_status_t moe_nvfp4_prepare_weight(int32_t which, const void* w, int32_t D, int32_t F, int32_t E, void* data,
+                                      size_t data_bytes, void* scales, size_t scale_bytes, moe_stream_t stream) {
+    size_t need_data = 0, need_scales = 0;
+    moe_status_t st = moe_nvfp4_weight_bytes(which, D, F, E, &need_data, &need_scales);
+    if (st != MOE_OK) return st;
+    if (!w || !data || !scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(data, 16) || !aligned(scales, 256)) return MOE_ERR_MISALIGNED;
+    if (data_bytes < need_data || scale_bytes < need_scales) return MOE_ERR_WORKSPACE_TOO_SMALL;
     DeviceInfo dev;
     if ((st = device_info(&dev)) != MOE_OK) return st;
     if (!dev.supported) return MOE_ERR_UNSUPPORTED_DEVICE;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    MxProblem p{};
-    p.T = T;
-    p.D = D;
-    p.F = F;
-    p.E = E;
-    p.K = K;
-    p.x = x;
-    p.ids = topk_ids;
-    p.scores = topk_scores;
-    p.scores_dtype = scores_dtype;
-    p.w13q = w13_data;
-    p.w13s = w13_scales;
-    p.w2q = w2_data;
-    p.w2s = w2_scales;
-    p.out = out;
-    p.status = reinterpret_cast<uint32_t*>(ws + L.off[MOE_MXWS_STATUS]);
-    p.counts = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_COUNTS]);
-    p.offsets = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_OFFSETS]);
-    p.tiles1 = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_TILES]);
-    p.tiles2 = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_TILES2]);
-    p.block_counts = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_BLOCK_COUNTS]);
-    p.block_bases = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_BLOCK_BASES]);
-    p.perm = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_PERM]);
-    p.inv = reinterpret_cast<int32_t*>(ws + L.off[MOE_MXWS_INV]);
-    p.xq = ws + L.off[MOE_MXWS_XQ];
-    p.xs = ws + L.off[MOE_MXWS_XS];
-    p.hq = ws + L.off[MOE_MXWS_HQ];
-    p.hs = ws + L.off[MOE_MXWS_HS];
-    p.y = ws + L.off[MOE_MXWS_Y];
-    p.nblk = L.nblk;
-    p.padded_rows = L.padded_rows;
-    p.sm_count = dev.sm_count;
-    return launch_mx_forward(p, stage_begin, stage_end, reinterpret_cast<cudaStream_t>(stream));
+    return launch_nv_prepare_weight(which, w, D, F, E, data, scales, need_scales, dev.sm_count,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_nvfp4_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K) {
+    MxLayout L;
+    if (T == 0 || !make_mx_layout(T, D, F, E, K, &L, true)) return 0;
+    return L.off[MOE_MXWS_TOTAL];
+}
+
+moe_status_t moe_nvfp4_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                        size_t* region_offsets) {
+    if (region_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_mx_shape(T, D, F, E, K);
+    if (st != MOE_OK) return st;
+    MxLayout L;
+    if (!make_mx_layout(T, D, F, E, K, &L, true)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    std::memcpy(region_offsets, L.off, sizeof(L.off));
+    return MOE_OK;
+}
+
+moe_status_t moe_routed_experts_fwd_nvfp4(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                          int32_t scores_dtype, const void* w13_data, const void* w13_scales,
+                                          const void* w2_data, const void* w2_scales, float x_scale, float h_scale,
+                                          void* out, int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                          void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return moe_fwd_nvfp4_stages(x, topk_ids, topk_scores, scores_dtype, w13_data, w13_scales, w2_data, w2_scales,
+                                x_scale, h_scale, out, T, D, F, E, K, 0, MOE_MX_STAGES, workspace, workspace_bytes,
+                                stream);
+}
+
+moe_status_t moe_fwd_nvfp4_stages(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                  int32_t scores_dtype, const void* w13_data, const void* w13_scales,
+                                  const void* w2_data, const void* w2_scales, float x_scale, float h_scale, void* out,
+                                  int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, int32_t stage_begin,
+                                  int32_t stage_end, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return block_scaled_stages(true, x, topk_ids, topk_scores, scores_dtype, w13_data, w13_scales, w2_data,
+                               w2_scales, x_scale, h_scale, out, T, D, F, E, K, stage_begin, stage_end, workspace,
+                               workspace_bytes, stream);
 }
 
 moe_status_t moe_get_status(const void* workspace, uint32_t* device_bits, moe_stream_t stream) {

@@ -165,10 +165,20 @@ struct MxProblem {
     int nblk;
     int64_t padded_rows;  // capacity of XQ / HQ: 128 * (ceil(R / 128) + min(E, R))
     int sm_count;
+    float act_scale_x, act_scale_h;  // NVFP4 only: the activations' tensor scales
 };
 // Stages [stage_begin, stage_end) of: 0 status + routing + gather-quantize, 1 gate/up GEMM,
 // 2 down GEMM, 3 combine.
 moe_status_t launch_mx_forward(const MxProblem& p, int stage_begin, int stage_end, cudaStream_t stream);
+
+// NVFP4 forward (nvfp4.cu): the same problem and stages, with packed E2M1 operands (cols / 2 bytes
+// per row) and UE4M3 scales per 16; a prepared weight's scale buffer starts with a 256-byte header
+// holding its fp32 tensor scale.
+size_t nv_weight_scale_bytes(int which, int32_t D, int32_t F, int32_t E);
+size_t nv_act_scale_bytes(int64_t padded_rows, int32_t cols);
+moe_status_t launch_nv_prepare_weight(int which, const void* w, int32_t D, int32_t F, int32_t E, void* data,
+                                      void* scales, size_t scale_bytes, int sm_count, cudaStream_t stream);
+moe_status_t launch_nv_forward(const MxProblem& p, int stage_begin, int stage_end, cudaStream_t stream);
 
 // The combine of the route-wise RMSNorm variant: out[t] = sum_k s * y / sqrt(mean(y^2) + eps).
 moe_status_t launch_combine_rmsnorm(const void* y, const int32_t* ids, const void* scores, int32_t scores_dtype,

@@ -24,7 +24,7 @@
 // 96 up rows, a down tile's rows 192 consecutive output rows.
 #include <cuda_fp8.h>
 
-#include "gemm_pipeline.cuh"
+#include "block_scaled.cuh"
 
 namespace moe {
 
@@ -50,9 +50,6 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, f
     const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c * m, d * m), __NV_SATFINITE, __NV_E4M3);
     return (lo & 0xffffu) | (hi << 16);
 }
-
-// Byte offset of row r (of a 128-row chunk) and block k (of 4) inside a scale chunk.
-__device__ __forceinline__ int sf_in_chunk(int r, int k) { return 16 * (r & 31) + 4 * ((r & 127) >> 5) + k; }
 
 // One warp quantizes one row of `cols` bf16 values (cols % 128 == 0; src null = a zero row) into
 // E4M3 codes at dst and UE8M0 scales: the four scales of 128-column group g go, as one 32-bit
@@ -161,27 +158,6 @@ __global__ void __launch_bounds__(256) k_mx_gather_quant(const uint4* __restrict
 
 // ------------------------------------------------------------------------------ tile policies
 
-struct MxTile {
-    int32_t e, n, row0, rows, rrow0, kblocks;  // row0: first padded row; rrow0: first routed row
-};
-
-// Tile list over padded rows: expert e owns (tiles[e+1] - tiles[e]) row tiles x ntn column tiles,
-// rows fastest, so CTAs running at the same time share one weight tile through L2.
-__device__ __forceinline__ MxTile decode_mx_tile(int32_t tile, const GemmArgs& a) {
-    MxTile t;
-    t.e = owning_expert(tile, a.tiles, a.ntn, a.E);
-    const int32_t first = __ldg(a.tiles + t.e);
-    const int32_t mt = __ldg(a.tiles + t.e + 1) - first;
-    const int32_t local = tile - a.ntn * first;
-    t.n = local / mt;
-    const int32_t m = local - t.n * mt;
-    t.row0 = kBM * (first + m);
-    t.rows = min(kBM, __ldg(a.counts + t.e) - m * kBM);
-    t.rrow0 = __ldg(a.offsets + t.e) + m * kBM;
-    t.kblocks = a.kblocks;
-    return t;
-}
-
 // Gate/up GEMM with SwiGLU and MX quantization of H: A = XQ rows (K = D), B = 96 gate rows and
 // the same 96 up rows of w13; the epilogue writes HQ codes and scales for all 128 rows of the tile
 // (padding rows come from zero XQ rows and give zero H rows).
@@ -288,13 +264,6 @@ struct MxDown {
         }
     }
 };
-
-int quant_grid(int64_t rows, int sm_count) {
-    const int64_t want = (rows + 7) / 8;  // 8 warps per block, one row each
-    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-    const int64_t g = want < cap ? want : cap;
-    return static_cast<int>(g > 0 ? g : 1);
-}
 
 }  // namespace
 

@@ -1,7 +1,7 @@
 // ptx_sm103.cuh -- inline-PTX wrappers for the Blackwell (sm_103a) asynchronous machinery used
 // by the grouped GEMMs: mbarriers (with bounded waits), TMA tensor loads, tcgen05 tensor-memory
-// allocation, tcgen05.mma (bf16 in, or block-scaled E4M3 in with tcgen05.cp of the scales; fp32
-// accumulate in TMEM), tcgen05.commit and tcgen05.ld.
+// allocation, tcgen05.mma (bf16 in, or block-scaled E4M3 / E2M1 in with tcgen05.cp of the scales;
+// fp32 accumulate in TMEM), tcgen05.commit and tcgen05.ld.
 //
 // Written from the public PTX ISA (tcgen05 / cp.async.bulk.tensor / mbarrier chapters). Every wait
 // here is bounded: it gives up after kWaitTimeoutNs of wall time, sets MOE_DEV_TIMEOUT in the
@@ -239,6 +239,26 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, ui
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma .kind::mxf4nvf4 with A and B E2M1 (format 1 at [7,10) and
+// [10,13)), both K-major, N >> 3 at [17,23), UE4M3 scales (bit 23 clear), M >> 4 at [24,29); the
+// scale-factor ids stay 0 (each MMA reads all four bytes of its scale column).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+    return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= (A * sfa) (B * sfb)^T for one M x N x 64 step of packed E2M1 operands (two per
+// byte, low nibble first) with one UE4M3 scale per row and 16 K elements (scale_vec::4X): a
+// 512-byte scale chunk in TMEM holds the four scales of each of 128 rows for this step.
+__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }

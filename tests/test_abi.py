@@ -219,3 +219,36 @@ def test_mxfp8_stage_range_validation(lib):
     assert st(3, 2) == INVALID
     assert st(2, 2) == OK  # an empty range enqueues nothing
     assert st(0, 4, T=0) == OK
+
+
+def test_nvfp4_host_validation_and_sizes(lib):
+    v = ctypes.c_void_p
+    f = ctypes.c_float
+    nv = lambda **kw: lib.moe_routed_experts_fwd_nvfp4(
+        v(FAKE), v(FAKE), v(FAKE), kw.get("sd", 0), v(kw.get("w13q", FAKE)), v(kw.get("w13s", FAKE)), v(FAKE),
+        v(FAKE), f(kw.get("gx", 0.01)), f(kw.get("gh", 0.01)), v(FAKE), kw.get("T", 16), kw.get("D", 256),
+        kw.get("F", 256), 8, 2, v(kw.get("ws", FAKE)), kw.get("wsb", 1 << 40), None)
+    assert nv(T=0) == OK
+    assert nv(gx=0.0) == INVALID
+    assert nv(gh=-1.0) == INVALID
+    assert nv(gx=float("inf")) == INVALID
+    assert nv(gh=float("nan")) == INVALID
+    assert nv(sd=5) == INVALID
+    assert nv(w13s=0) == INVALID
+    assert nv(D=192) == SHAPE
+    assert nv(w13s=FAKE + 16) == MISALIGNED
+    assert nv(ws=FAKE + 32) == MISALIGNED
+    need = binding.moe_nvfp4_workspace_bytes(16, 256, 256, 8, 2)
+    assert nv(wsb=need - 1) == WS_SMALL
+    for D, F, E in ((2048, 1408, 64), (7168, 2048, 256), (640, 384, 3)):
+        nd, ns = binding.moe_nvfp4_weight_bytes(binding.MOE_WEIGHT_W13, D, F, E)
+        assert nd == E * 2 * F * D // 2 and ns == 256 + E * -(-F // 64) * (-(-D // 256) * 4) * 512
+        nd, ns = binding.moe_nvfp4_weight_bytes(binding.MOE_WEIGHT_W2, D, F, E)
+        assert nd == E * D * F // 2 and ns == 256 + E * -(-D // 128) * (-(-F // 256) * 4) * 512
+    T, D, F, E, K = 4096, 2048, 1408, 64, 6
+    lay = binding.moe_nvfp4_workspace_layout(T, D, F, E, K)
+    rp = 128 * (-(-T * K // 128) + E)
+    assert lay["xs"] - lay["xq"] >= rp * D // 2 and lay["hs"] - lay["hq"] >= rp * F // 2
+    assert lay["hq"] - lay["xs"] >= rp // 128 * (-(-D // 256) * 4) * 512
+    assert lay["y"] - lay["hs"] >= rp // 128 * (-(-F // 256) * 4) * 512
+    assert lay["total"] == binding.moe_nvfp4_workspace_bytes(T, D, F, E, K)

@@ -6,10 +6,11 @@ row gather), the gate/up grouped GEMM with SwiGLU, the down grouped GEMM with th
 weighting, and the combine -- through the C ABI, on inputs already resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
-                    [--precision bf16|mxfp8] [--pass fwd|bwd]
+                    [--precision bf16|mxfp8|nvfp4] [--pass fwd|bwd]
 
---precision mxfp8 runs the block-scaled forward (E4M3 operands with UE8M0 scales, weights prepared
-once before the timed region, activations quantized inside each step).
+--precision mxfp8 / nvfp4 runs a block-scaled forward (E4M3 operands with UE8M0 scales per 32, or
+E2M1 with UE4M3 scales per 16 and tensor scales; weights prepared once before the timed region,
+activations quantized inside each step).
 
 Prints ONE JSON line (rank 0). Under torchrun each rank runs its own replica of the workload
 (tokens drawn with a rank-specific seed, the same weights): the path has no exchange step on one
@@ -44,6 +45,16 @@ L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 STAGES = ("dispatch", "gemm1_swiglu", "gemm2_score", "combine")
 KERNELS_PER_STEP = 7  # hist, scan, permute, gather, gemm1, gemm2, combine
 
+# Operand formats of the forward: bytes per quantized element (codes + scales), the tensor peak as
+# a multiple of the measured bf16 peak (nominal dense ratios: fp8 4.5 / 2.25, fp4 13.5 / 2.25), the
+# dtype label and the key prefix of recorded traffic.
+PRECISIONS = {
+    "bf16": {"elem_bytes": 2.0, "tensor_scale": 1.0, "dtype": "bf16", "key": ""},
+    "mxfp8": {"elem_bytes": 1.0 + 1.0 / 32, "tensor_scale": 2.0, "dtype": "mxfp8-e4m3", "key": "mx_"},
+    "nvfp4": {"elem_bytes": 0.5 + 1.0 / 16, "tensor_scale": 6.0, "dtype": "nvfp4-e2m1", "key": "nv_"},
+}
+NV_H_SCALE = 2.0 ** -8  # NVFP4 tensor scale of the SwiGLU output (|h| < 6 * 448 * 2^-8 = 10.5 here)
+
 
 # ------------------------------------------------------------------------------ host logic
 
@@ -54,8 +65,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--config", default="medium", choices=["tiny", "medium", "decode", "large", "skewed"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8"],
-                   help="forward operands: bf16, or MXFP8 E4M3 with prepared weights")
+    p.add_argument("--precision", default="bf16", choices=sorted(PRECISIONS),
+                   help="forward operands: bf16, MXFP8 E4M3 or NVFP4 E2M1 (block-scaled, prepared weights)")
     p.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
                    help="fwd: the forward layer (the headline); bwd: its backward pass (one call per step)")
     p.add_argument("--seed", type=int, default=0)
@@ -118,12 +129,11 @@ def measured_peaks() -> tuple[dict, str]:
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_costs(T, D, F, E, K, touched, mx=False):
-    """Algorithmic flops and bytes per launch of each stage (tile padding not counted). With mx the
-    operands are E4M3 bytes plus one UE8M0 scale byte per 32 (1 + 1/32 bytes per element)."""
+def kernel_costs(T, D, F, E, K, touched, q=None):
+    """Algorithmic flops and bytes per launch of each stage (tile padding not counted). q: bytes per
+    element of the block-scaled operands (codes + scales), None for the bf16 forward."""
     R = T * K
-    if mx:
-        q = 1.0 + 1.0 / 32
+    if q is not None:
         return {
             "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + R * D * 2 + R * D * q},
             "gemm1_swiglu": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * q + R * D * q + R * F * q},
@@ -138,18 +148,13 @@ def kernel_costs(T, D, F, E, K, touched, mx=False):
     }
 
 
-def path_costs(T, D, F, E, K, touched, mx=False):
+def path_costs(T, D, F, E, K, touched, wbytes=2.0):
     """The layer's algorithmic flops and bytes: touched experts' weights, x, out, ids, scores."""
-    wbytes = (1.0 + 1.0 / 32) if mx else 2
     return 6 * T * K * D * F, touched * 3 * F * D * wbytes + 2 * T * D * 2 + T * K * 8
 
 
-# Dense fp8 (E4M3, block-scaled) over dense bf16 tensor throughput, nominal (4.5 / 2.25 PFLOP/s).
-FP8_OVER_BF16 = 2.0
-
-
 def roofline_entry(name, costs, seconds, peaks, sustained, traffic, tensor_scale=1.0):
-    """tensor_scale multiplies the measured bf16 peak for another operand type (FP8_OVER_BF16)."""
+    """tensor_scale multiplies the measured bf16 peak for another operand type (PRECISIONS)."""
     c = costs[name]
     ridge = tensor_scale * peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if c["flops"] > 0 and c["flops"] / max(c["bytes"], 1) >= ridge:
@@ -157,7 +162,7 @@ def roofline_entry(name, costs, seconds, peaks, sustained, traffic, tensor_scale
         achieved = c["flops"] / seconds / 1e12
         kind = "sustained" if sustained else "burst"
         if tensor_scale != 1.0:
-            kind += f" bf16 x {tensor_scale:g} (fp8/bf16 nominal ratio)"
+            kind += f" bf16 x {tensor_scale:g} (nominal dense ratio of the operand type to bf16)"
         return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": name, "peak_kind": kind}
     achieved = c["bytes"] / seconds / 1e9
@@ -171,6 +176,8 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in ("mixture_experts_routed_topk_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_routed_topk_gb300/csrc/mxfp8.cu",
+                "mixture_experts_routed_topk_gb300/csrc/nvfp4.cu",
+                "mixture_experts_routed_topk_gb300/csrc/block_scaled.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/gemm_pipeline.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/ptx_sm103.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/routing.cu",
@@ -303,7 +310,10 @@ def time_oracle(sample, nthreads: int) -> float:
     import oracle
 
     t0 = time.perf_counter()
-    if "w13_mx" in sample:
+    if "w13_nv" in sample:
+        oracle.routed_experts_nvfp4(sample["x"], sample["ids"], sample["scores"], sample["w13_nv"],
+                                    sample["w2_nv"], sample["gx"], sample["gh"], nthreads=nthreads)
+    elif "w13_mx" in sample:
         oracle.routed_experts_mxfp8(sample["x"], sample["ids"], sample["scores"], sample["w13_mx"],
                                     sample["w2_mx"], nthreads=nthreads)
     else:
@@ -312,19 +322,30 @@ def time_oracle(sample, nthreads: int) -> float:
     return time.perf_counter() - t0
 
 
-def cpu_baseline(d, wl, name: str, target_s: float, mx: bool = False) -> dict:
-    """The oracle as it stands on the host cores: a bounded token sample, repeated to fill about
-    target_s seconds; tokens/s = tokens processed / seconds. With mx, the oracle's MXFP8 forward on
-    weights the oracle quantized beforehand (not timed, as the weights are prepared once)."""
-    cores = os.cpu_count() or 1
-    ids_host = d["topk_ids"].cpu().numpy()
-    n_tok = bounded_tokens(ids_host, wl, oracle_tokens_for(target_s, wl, cores, 0.35 if mx else 0.7))
-    sample = oracle_sample(d, n_tok)
-    if mx:
-        import oracle
+def prepare_oracle_sample(sample, precision: str, gx: float = 0.0):
+    """Quantized weights for the oracle's block-scaled forwards (prepared once, not timed). The
+    NVFP4 weight scales come from the sample's experts."""
+    import oracle
 
+    if precision == "mxfp8":
         sample["w13_mx"] = oracle.mx_quantize_rows(sample["w13"])
         sample["w2_mx"] = oracle.mx_quantize_rows(sample["w2"])
+    elif precision == "nvfp4":
+        sample["w13_nv"] = oracle.nvfp4_prepare(sample["w13"])
+        sample["w2_nv"] = oracle.nvfp4_prepare(sample["w2"])
+        sample["gx"], sample["gh"] = gx, NV_H_SCALE
+
+
+def cpu_baseline(d, wl, name: str, target_s: float, precision: str = "bf16", gx: float = 0.0) -> dict:
+    """The oracle as it stands on the host cores: a bounded token sample, repeated to fill about
+    target_s seconds; tokens/s = tokens processed / seconds. For a block-scaled precision, the
+    oracle's forward of that format on weights it quantized beforehand."""
+    cores = os.cpu_count() or 1
+    ids_host = d["topk_ids"].cpu().numpy()
+    rate = 0.7 if precision == "bf16" else 0.35
+    n_tok = bounded_tokens(ids_host, wl, oracle_tokens_for(target_s, wl, cores, rate))
+    sample = oracle_sample(d, n_tok)
+    prepare_oracle_sample(sample, precision, gx)
     secs = [time_oracle(sample, cores)]
     reps = max(1, min(100, int(target_s / max(secs[0], 1e-6))))
     secs += [time_oracle(sample, cores) for _ in range(reps - 1)]
@@ -358,11 +379,19 @@ def run_ours(args, rank, world, local_rank):
     scores = W.make_scores(T, K, wl.scores, rseed, device)
     w13, w2 = W.make_weights(E, D, F, args.seed, device)
     dims = (T, D, F, E, K)
+    prec = PRECISIONS[args.precision]
     mx = args.precision == "mxfp8"
+    nv = args.precision == "nvfp4"
+    gx = 0.0
     if mx:  # prepared once, as the pages prepare block-scaled weights before execution
         w13_mx = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W13, w13)
         w2_mx = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W2, w2)
         ws = binding.alloc_workspace(binding.moe_mxfp8_workspace_bytes(*dims), device)
+    elif nv:  # weights prepared once; x's tensor scale calibrated from this batch, h's a constant
+        w13_nv = binding.moe_nvfp4_prepare_weight(binding.MOE_WEIGHT_W13, w13)
+        w2_nv = binding.moe_nvfp4_prepare_weight(binding.MOE_WEIGHT_W2, w2)
+        gx = float(torch.tensor(x.abs().max().float().item(), dtype=torch.float32) / 2688.0)
+        ws = binding.alloc_workspace(binding.moe_nvfp4_workspace_bytes(*dims), device)
     else:
         ws = binding.alloc_workspace(binding.moe_workspace_bytes(*dims), device)
     out = torch.empty((T, D), dtype=torch.bfloat16, device=device)
@@ -370,11 +399,15 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(device)
 
     def step(ev=None):
-        if mx:
+        if mx or nv:
             for s in range(binding.MX_STAGES):
                 if ev is not None:
                     ev[s].record(stream)
-                binding.moe_fwd_mxfp8_stages(x, ids, scores, w13_mx, w2_mx, out, ws, (F, E), s, s + 1, stream)
+                if mx:
+                    binding.moe_fwd_mxfp8_stages(x, ids, scores, w13_mx, w2_mx, out, ws, (F, E), s, s + 1, stream)
+                else:
+                    binding.moe_fwd_nvfp4_stages(x, ids, scores, w13_nv, w2_nv, out, ws, (F, E), gx, NV_H_SCALE, s,
+                                                 s + 1, stream)
             if ev is not None:
                 ev[binding.MX_STAGES].record(stream)
             return
@@ -400,7 +433,8 @@ def run_ours(args, rank, world, local_rank):
     status = binding.moe_get_status(ws, stream)
     if status != 0:
         raise RuntimeError(f"device status bits {status:#x} after warm-up")
-    counts = binding.moe_mxfp8_workspace_layout(*dims) if mx else binding.moe_workspace_layout(*dims)
+    counts = (binding.moe_mxfp8_workspace_layout(*dims) if mx else
+              binding.moe_nvfp4_workspace_layout(*dims) if nv else binding.moe_workspace_layout(*dims))
     cnt = ws[counts["counts"]:counts["counts"] + 4 * E].view(torch.int32)
     touched = int((cnt > 0).sum().item())
 
@@ -464,6 +498,9 @@ def run_ours(args, rank, world, local_rank):
             if mx:
                 binding.moe_routed_experts_fwd_mxfp8(x_d[b], ids_d[b], scores_d[b], w13_mx, w2_mx, out_d[b], ws,
                                                      (F, E), stream)
+            elif nv:
+                binding.moe_routed_experts_fwd_nvfp4(x_d[b], ids_d[b], scores_d[b], w13_nv, w2_nv, out_d[b], ws,
+                                                     (F, E), gx, NV_H_SCALE, stream)
             else:
                 binding.moe_routed_experts_fwd(x_d[b], ids_d[b], scores_d[b], w13, w2, out_d[b], ws, stream)
             computed[b].record(stream)
@@ -497,23 +534,23 @@ def run_ours(args, rank, world, local_rank):
         return
 
     peaks, peak_src = measured_peaks()
-    costs = kernel_costs(T, D, F, E, K, touched, mx)
+    costs = kernel_costs(T, D, F, E, K, touched, None if args.precision == "bf16" else prec["elem_bytes"])
     mean_stage = {s: statistics.mean(v) for s, v in stage_ms.items()}
     dominant = max(mean_stage, key=mean_stage.get)
     ms_per_step = total_s * 1e3 / args.steps
     sustained = ms_per_step * args.steps > 2000.0  # a seconds-long loop runs under the power cap
-    tensor_scale = FP8_OVER_BF16 if mx else 1.0
+    tensor_scale = prec["tensor_scale"]
     roof = roofline_entry(dominant, costs, mean_stage[dominant] / 1e3, peaks, sustained,
-                          recorded_traffic(args.config, ("mx_" if mx else "") + dominant), tensor_scale)
+                          recorded_traffic(args.config, prec["key"] + dominant), tensor_scale)
     roof["peak_source"] = peak_src
-    flops, alg_bytes = path_costs(T, D, F, E, K, touched, mx)
+    flops, alg_bytes = path_costs(T, D, F, E, K, touched, prec["elem_bytes"])
     step_s = ms_per_step / 1e3
     t_roof = max(flops / (tensor_scale * peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
 
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline({"x": x, "topk_ids": ids, "topk_scores": scores, "w13": w13, "w2": w2}, wl,
-                           args.config, args.cpu_seconds, mx)
+                           args.config, args.cpu_seconds, args.precision, gx)
 
     line = assemble_line(
         metric=METRIC,
@@ -526,7 +563,7 @@ def run_ours(args, rank, world, local_rank):
         higher_is_better=True,
         scaling="weak",
         vs_baseline=None,
-        dtype="mxfp8-e4m3" if mx else "bf16",
+        dtype=prec["dtype"],
         data="synthetic",
         config={"workload": args.config if not args.tokens else f"{args.config} (T={T})", "T": T, "D": D, "F": F,
                 "precision": args.precision,
@@ -651,16 +688,15 @@ def run_reference(args, rank, world, local_rank):
     x = W.make_x(T, D, args.seed, dev)
     ids = W.make_topk_ids(T, E, K, wl.routing, args.seed, dev)
     scores = W.make_scores(T, K, wl.scores, args.seed, dev)
-    mx = args.precision == "mxfp8"
-    n_tok = bounded_tokens(ids.cpu().numpy(), wl, oracle_tokens_for(per_step_s, wl, cores, 0.35 if mx else 0.7))
+    rate = 0.7 if args.precision == "bf16" else 0.35
+    n_tok = bounded_tokens(ids.cpu().numpy(), wl, oracle_tokens_for(per_step_s, wl, cores, rate))
     first = ids[:n_tok].cpu()
     experts = sorted(set(first[(first >= 0) & (first < E)].tolist()))
     w13, w2 = W.make_weights(E, D, F, args.seed, dev, experts=experts)
     sample = oracle_sample({"x": x, "topk_ids": ids, "topk_scores": scores, "w13": w13, "w2": w2}, n_tok)
     del w13, w2
-    if mx:  # weights prepared once, outside the timed steps
-        sample["w13_mx"] = oracle.mx_quantize_rows(sample["w13"])
-        sample["w2_mx"] = oracle.mx_quantize_rows(sample["w2"])
+    gx = float(torch.tensor(x.abs().max().float().item(), dtype=torch.float32) / 2688.0)
+    prepare_oracle_sample(sample, args.precision, gx)  # weights prepared once, outside the timed steps
     for _ in range(max(args.warmup, 0)):
         time_oracle(sample, cores)
     secs = [time_oracle(sample, cores) for _ in range(args.steps)]

@@ -1,6 +1,6 @@
 /*
- * moe_routed_experts.h -- C ABI of the routed top-k mixture-of-experts expert layer (forward pass)
- * for NVIDIA GB300 (sm_103a).
+ * moe_routed_experts.h -- C ABI of the routed top-k mixture-of-experts expert layer (forward,
+ * backward and block-scaled forwards) for NVIDIA GB300 (sm_103a).
  *
  * The layer (the expert path shared by the TeraMoE README, Dist-MoE 0.1.0 and the Primus MegaMoE
  * guide; the MoonEP page describes its weight layout):
@@ -396,7 +396,9 @@ moe_status_t moe_nvfp4_prepare_weight(int32_t which, const void *w, int32_t D, i
 /* Bytes of device workspace of the NVFP4 forward, and its layout: the MOE_MXWS_* regions, with XQ
  * and HQ holding packed E2M1 codes ([Rp, D/2] and [Rp, F/2] bytes) and XS and HS UE4M3 scales
  * (padded row p, 16-block b at byte ((p/128) * P(cols) + b/4) * 512 + 16 (p%32) + 4 ((p%128)/32)
- * + b%4). Pure arithmetic. */
+ * + b%4). The padding rows after each expert's rows have zero scales in XS and zero codes and
+ * scales in HQ / HS; their XQ codes are left unwritten (a zero scale makes them contribute 0).
+ * Pure arithmetic. */
 size_t moe_nvfp4_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K);
 moe_status_t moe_nvfp4_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
                                         size_t *region_offsets);

@@ -51,18 +51,25 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, f
     return (lo & 0xffffu) | (hi << 16);
 }
 
-// One warp quantizes one row of `cols` bf16 values (cols % 128 == 0; src null = a zero row) into
+// One warp quantizes one row of `cols` bf16 values (cols % 128 == 0; src null = a zero row: zero
+// codes and the all-zero block's scale code 0, written directly) into
 // E4M3 codes at dst and UE8M0 scales: the four scales of 128-column group g go, as one 32-bit
 // word, to sf_row + g * sf_group_stride. Lane l handles 8 consecutive values per 256-column step;
 // lanes 4j .. 4j+3 share one 32-value block.
 __device__ __forceinline__ void warp_quantize_row(const uint4* src, uint8_t* dst, int cols, uint8_t* sf_row,
                                                   int64_t sf_group_stride) {
     const int lane = threadIdx.x & 31;
+    if (src == nullptr) {  // a zero row: codes 0 and scale codes 0 (e = -127), no arithmetic
+        for (int c = lane * 16; c < cols; c += 512) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+        for (int g = lane; g < cols / 128; g += 32)
+            *reinterpret_cast<uint32_t*>(sf_row + static_cast<int64_t>(g) * sf_group_stride) = 0u;
+        return;
+    }
     for (int c0 = 0; c0 < cols; c0 += 256) {
         const int c = c0 + lane * 8;
         const bool active = c < cols;
         float v[8];
-        if (active && src != nullptr) {
+        if (active) {
             const uint4 q = __ldg(src + c / 8);
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -137,15 +144,25 @@ __global__ void __launch_bounds__(256) k_mx_gather_quant(const uint4* __restrict
                                                          const int32_t* __restrict__ tiles, int32_t E, int32_t K,
                                                          int32_t D, uint8_t* __restrict__ xq,
                                                          uint8_t* __restrict__ xs) {
+    extern __shared__ int32_t s_tiles[];  // tiles[0 .. E], so each row's expert lookup stays on chip
     griddep_wait();
     griddep_launch_dependents();
-    const int64_t rows = 128 * static_cast<int64_t>(__ldg(tiles + E));
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_tiles[i] = __ldg(tiles + i);
+    __syncthreads();
+    const int64_t rows = 128 * static_cast<int64_t>(s_tiles[E]);
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int groups = D / 128;
     for (int64_t prow = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); prow < rows;
          prow += warps_total) {
-        const int32_t e = owning_expert(static_cast<int32_t>(prow >> 7), tiles, 1, E);
-        const int64_t i = prow - 128 * static_cast<int64_t>(__ldg(tiles + e));
+        const int32_t tile = static_cast<int32_t>(prow >> 7);
+        int lo = 0, hi = E - 1;  // the last expert e with tiles[e] <= tile (empty experts are skipped)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_tiles[mid] <= tile) lo = mid;
+            else hi = mid - 1;
+        }
+        const int32_t e = lo;
+        const int64_t i = prow - 128 * static_cast<int64_t>(s_tiles[e]);
         const uint4* src = nullptr;
         if (i < __ldg(counts + e)) {
             const int32_t p = __ldg(perm + __ldg(offsets + e) + i);
@@ -301,7 +318,8 @@ moe_status_t mx_dispatch(const MxProblem& p, cudaStream_t stream) {
     b.status = p.status;
     moe_status_t st = launch_routing(b, stream);
     if (st != MOE_OK) return st;
-    return launch_pdl(k_mx_gather_quant, dim3(quant_grid(p.padded_rows, p.sm_count)), dim3(256), 0, stream,
+    return launch_pdl(k_mx_gather_quant, dim3(quant_grid(p.padded_rows, p.sm_count)), dim3(256),
+                      sizeof(int32_t) * (p.E + 1), stream,
                       static_cast<const uint4*>(p.x), static_cast<const int32_t*>(p.perm),
                       static_cast<const int32_t*>(p.counts), static_cast<const int32_t*>(p.offsets),
                       static_cast<const int32_t*>(p.tiles1), p.E, p.K, p.D, p.xq, p.xs) == cudaSuccess

@@ -67,19 +67,26 @@ __device__ __forceinline__ uint32_t nv_block(const float (&v)[16], float G, floa
     return s;
 }
 
-// One warp quantizes one row of `cols` bf16 values (cols % 128 == 0; src null = a zero row) into
-// packed E2M1 codes at dst (cols / 2 bytes) and UE4M3 scales: the four scales of 64-column group g
-// go, as one 32-bit word, to sf_row + g * sf_group_stride, for g < nv_groups(cols) (zero words for
-// the padding groups). Lane l handles 16 consecutive values per 512-column step.
+// One warp quantizes one row of `cols` bf16 values (cols % 128 == 0) into packed E2M1 codes at dst
+// (cols / 2 bytes) and UE4M3 scales: the four scales of 64-column group g go, as one 32-bit word,
+// to sf_row + g * sf_group_stride, for g < nv_groups(cols) (zero words for the padding groups).
+// src null marks a padding row: its scales are written as zero and its codes are left as they are
+// (a zero block scale makes every product of the row exactly 0, and E2M1 has no NaN). Lane l
+// handles 16 consecutive values per 512-column step.
 __device__ __forceinline__ void warp_quantize_row_nv(const uint4* src, uint8_t* dst, int cols, float G, float t6g,
                                                      uint8_t* sf_row, int64_t sf_group_stride) {
     const int lane = threadIdx.x & 31;
+    if (src == nullptr) {  // a padding row: zero scale words only
+        for (int g = lane; g < nv_groups(cols); g += 32)
+            *reinterpret_cast<uint32_t*>(sf_row + static_cast<int64_t>(g) * sf_group_stride) = 0u;
+        return;
+    }
     const int cols_pad = nv_groups(cols) * 64;
     for (int c0 = 0; c0 < cols_pad; c0 += 512) {
         const int c = c0 + lane * 16;
         const bool data = c < cols;
         float v[16];
-        if (data && src != nullptr) {
+        if (data) {
             const uint4 q0 = __ldg(src + c / 8), q1 = __ldg(src + c / 8 + 1);
             const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
@@ -175,23 +182,34 @@ __global__ void __launch_bounds__(256) k_nv_prepare_weight(const uint4* __restri
 }
 
 // XQ[prow] = NVFP4(x[t], G_x) for every padded row (routed row offsets[e] + i of expert e at
-// prow = 128 tiles[e] + i when i < counts[e], zeros otherwise). One warp per padded row.
+// prow = 128 tiles[e] + i when i < counts[e]); padding rows get zero scales (their codes are not
+// written). One warp per padded row.
 __global__ void __launch_bounds__(256) k_nv_gather_quant(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                                                          const int32_t* __restrict__ counts,
                                                          const int32_t* __restrict__ offsets,
                                                          const int32_t* __restrict__ tiles, int32_t E, int32_t K,
                                                          int32_t D, float gx, uint8_t* __restrict__ xq,
                                                          uint8_t* __restrict__ xs) {
+    extern __shared__ int32_t s_tiles[];  // tiles[0 .. E], so each row's expert lookup stays on chip
     griddep_wait();
     griddep_launch_dependents();
-    const int64_t rows = 128 * static_cast<int64_t>(__ldg(tiles + E));
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_tiles[i] = __ldg(tiles + i);
+    __syncthreads();
+    const int64_t rows = 128 * static_cast<int64_t>(s_tiles[E]);
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int groups = nv_groups(D);
     const float t6g = __fmul_rn(6.0f, gx);
     for (int64_t prow = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); prow < rows;
          prow += warps_total) {
-        const int32_t e = owning_expert(static_cast<int32_t>(prow >> 7), tiles, 1, E);
-        const int64_t i = prow - 128 * static_cast<int64_t>(__ldg(tiles + e));
+        const int32_t tile = static_cast<int32_t>(prow >> 7);
+        int lo = 0, hi = E - 1;  // the last expert e with tiles[e] <= tile (empty experts are skipped)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_tiles[mid] <= tile) lo = mid;
+            else hi = mid - 1;
+        }
+        const int32_t e = lo;
+        const int64_t i = prow - 128 * static_cast<int64_t>(s_tiles[e]);
         const uint4* src = nullptr;
         if (i < __ldg(counts + e)) {
             const int32_t p = __ldg(perm + __ldg(offsets + e) + i);
@@ -338,7 +356,8 @@ moe_status_t nv_dispatch(const MxProblem& p, cudaStream_t stream) {
     b.status = p.status;
     moe_status_t st = launch_routing(b, stream);
     if (st != MOE_OK) return st;
-    return launch_pdl(k_nv_gather_quant, dim3(quant_grid(p.padded_rows, p.sm_count)), dim3(256), 0, stream,
+    return launch_pdl(k_nv_gather_quant, dim3(quant_grid(p.padded_rows, p.sm_count)), dim3(256),
+                      sizeof(int32_t) * (p.E + 1), stream,
                       static_cast<const uint4*>(p.x), static_cast<const int32_t*>(p.perm),
                       static_cast<const int32_t*>(p.counts), static_cast<const int32_t*>(p.offsets),
                       static_cast<const int32_t*>(p.tiles1), p.E, p.K, p.D, p.act_scale_x, p.xq, p.xs) == cudaSuccess

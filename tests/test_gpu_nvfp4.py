@@ -187,7 +187,7 @@ def test_nvfp4_forward_matches_oracle(name):
     assert err <= OUT_TOL, (name, err)
 
 
-def test_activation_rows_bit_exact_and_padding_zero():
+def test_activation_rows_bit_exact_and_padding_scales_zero():
     T, D, F, E, K = 300, 640, 256, 6, 3  # D leaves two padding scale groups per row
     d = problem(T, D, F, E, K, seed=4)
     out, ws = run_nv(d)
@@ -210,7 +210,8 @@ def test_activation_rows_bit_exact_and_padding_zero():
         valid_rows.append(prows)
     used = 128 * int(tiles[E])
     pad = np.setdiff1d(np.arange(used), np.concatenate(valid_rows))
-    assert pad.size > 0 and not xq[pad].any() and not untile_act_scales(xs, pad, D).any()
+    # padding rows: zero scales (their codes are not written: a zero scale makes them contribute 0)
+    assert pad.size > 0 and not untile_act_scales(xs, pad, D).any()
     # the padding scale groups (K values D .. 768) of every used row tile are zero
     grid = xs[:used // 128 * groups(D) * 512].reshape(used // 128, groups(D), 512)
     assert not grid[:, D // 64:].any()

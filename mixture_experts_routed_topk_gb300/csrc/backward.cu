@@ -381,27 +381,33 @@ struct BwdWgrad {
         for (int j = 0; j < kBRows / 64; ++j) tma_load_2d(sb + j * kMnBoxBytes, tb, bar, t.n * kBRows + 64 * j, k);
     }
 
-    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4*, const GemmArgs& a) {
+    // The tile's K is one expert's padded rows (a few hundred at most sizes), so its mainloop is
+    // short and the 64 KB of gradient it writes decide the pace: rows leave through the per-warp
+    // staging buffer, so each store instruction writes four whole 128-byte row segments instead
+    // of 32 scattered 16-byte pieces.
+    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4* stage, const GemmArgs& a) {
         const int32_t r = t.m * kBM + row_in_tile;
         __nv_bfloat16* dst = a.out0 + (static_cast<int64_t>(t.e) * a.mdim + r) * a.ndim;
+        uint32_t words[32];  // 64 bf16 of this thread's row: two 32-column chunks
 #pragma unroll 1
-        for (int c = 0; c < kBRows / 32; ++c) {
-            __syncwarp();
-            uint32_t v[32];
-            if (t.kblocks > 0) {  // warp-uniform
-                tmem_ld_32cols(taddr + c * 32, v);
-                tmem_ld_wait(v);
-            } else {
+        for (int cp = 0; cp < kBRows / 64; ++cp) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0u;
-            }
-            const int32_t c0 = t.n * kBRows + c * 32;
-            if (r < a.mdim && c0 < a.ndim) {
-                uint32_t w[16];
+            for (int half = 0; half < 2; ++half) {
+                __syncwarp();
+                uint32_t v[32];
+                if (t.kblocks > 0) {  // warp-uniform
+                    tmem_ld_32cols(taddr + (2 * cp + half) * 32, v);
+                    tmem_ld_wait(v);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                store_64B(dst + c0, w);
+                    for (int j = 0; j < 32; ++j) v[j] = 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    words[half * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
             }
+            const int32_t c0 = t.n * kBRows + cp * 64;  // ndim % 64 == 0: the 64 columns are all in or all out
+            warp_store_row_segments(stage, words, reinterpret_cast<char*>(dst + c0), r < a.mdim && c0 < a.ndim);
         }
     }
 };

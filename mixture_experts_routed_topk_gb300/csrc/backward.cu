@@ -189,35 +189,50 @@ struct BwdRecompute {
         tma_load_2d(sb + kBBytes / 2, tb, bar, kb * kBK, gate + a.F);
     }
 
-    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4*, const GemmArgs& a) {
+    // Rows leave through the per-warp staging buffer in 64-column groups (F % 64 == 0: a group is all
+    // in or all out), so each store instruction writes four whole 128-byte row segments.
+    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4* stage, const GemmArgs& a) {
         const int64_t row = static_cast<int64_t>(t.row0) + row_in_tile;
         const int32_t pair = __ldg(a.pperm + row);
         const float s = pair >= 0 ? pair_score(a, pair) : 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < kBN1 / 32; ++c) {
+        for (int cp = 0; cp < kBN1 / 64; ++cp) {
             __syncwarp();
-            uint32_t g[32], u[32];
-            tmem_ld_32cols(taddr + c * 32, g);
-            tmem_ld_32cols(taddr + kBN1 + c * 32, u);
-            tmem_ld_wait(g);
-            tmem_ld_tie(u);
-            const int32_t f0 = t.n * kBN1 + c * 32;
-            if (f0 < a.F) {
-                uint32_t wg[16], wu[16], wh[16];
+            uint32_t g0[32], g1[32], u0[32], u1[32];
+            tmem_ld_32cols(taddr + cp * 64, g0);
+            tmem_ld_32cols(taddr + cp * 64 + 32, g1);
+            tmem_ld_32cols(taddr + kBN1 + cp * 64, u0);
+            tmem_ld_32cols(taddr + kBN1 + cp * 64 + 32, u1);
+            tmem_ld_wait(g0);
+            tmem_ld_tie(g1);
+            tmem_ld_tie(u0);
+            tmem_ld_tie(u1);
+            const int32_t f0 = t.n * kBN1 + cp * 64;
+            const bool ok = f0 < a.F;  // warp-uniform
+            uint32_t w[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-                    const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-                    float sg;
-                    const float a0 = silu_of(g0, &sg), a1 = silu_of(g1, &sg);
-                    wg[j] = pack_bf16x2(g0, g1);
-                    wu[j] = pack_bf16x2(u0, u1);
-                    wh[j] = pack_bf16x2(s * a0 * u0, s * a1 * u1);
-                }
-                store_64B(a.out0 + row * 2 * a.F + f0, wg);
-                store_64B(a.out0 + row * 2 * a.F + a.F + f0, wu);
-                store_64B(a.out1 + row * a.F + f0, wh);
+            for (int j = 0; j < 16; ++j) {
+                w[j] = pack_bf16x2(__uint_as_float(g0[2 * j]), __uint_as_float(g0[2 * j + 1]));
+                w[16 + j] = pack_bf16x2(__uint_as_float(g1[2 * j]), __uint_as_float(g1[2 * j + 1]));
             }
+            warp_store_row_segments(stage, w, reinterpret_cast<char*>(a.out0 + row * 2 * a.F + f0), ok);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                w[j] = pack_bf16x2(__uint_as_float(u0[2 * j]), __uint_as_float(u0[2 * j + 1]));
+                w[16 + j] = pack_bf16x2(__uint_as_float(u1[2 * j]), __uint_as_float(u1[2 * j + 1]));
+            }
+            warp_store_row_segments(stage, w, reinterpret_cast<char*>(a.out0 + row * 2 * a.F + a.F + f0), ok);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float sg;
+                const float ga = __uint_as_float(g0[2 * j]), gb = __uint_as_float(g0[2 * j + 1]);
+                const float gc = __uint_as_float(g1[2 * j]), gd = __uint_as_float(g1[2 * j + 1]);
+                w[j] = pack_bf16x2(s * silu_of(ga, &sg) * __uint_as_float(u0[2 * j]),
+                                   s * silu_of(gb, &sg) * __uint_as_float(u0[2 * j + 1]));
+                w[16 + j] = pack_bf16x2(s * silu_of(gc, &sg) * __uint_as_float(u1[2 * j]),
+                                        s * silu_of(gd, &sg) * __uint_as_float(u1[2 * j + 1]));
+            }
+            warp_store_row_segments(stage, w, reinterpret_cast<char*>(a.out1 + row * a.F + f0), ok);
         }
     }
 };
@@ -242,69 +257,51 @@ struct BwdDgradDown {
             tma_load_2d(sb + j * kMnBoxBytes, tb, bar, t.n * kBN2 + 64 * j, t.e * a.D + kb * kBK);
     }
 
-    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4*, const GemmArgs& a) {
+    // Per 64-column group (F % 64 == 0: all in or all out): this warp's 32 rows of g and u come in
+    // with coalesced loads through the staging buffer, dg and du leave the same way, so every load
+    // and store instruction moves four whole 128-byte row segments.
+    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4* stage, const GemmArgs& a) {
+        const int lane = threadIdx.x & 31;
         const int64_t row = static_cast<int64_t>(t.row0) + row_in_tile;
         const int32_t pair = __ldg(a.pperm + row);
         const float s = pair >= 0 ? pair_score(a, pair) : 0.0f;
-        // this row's g and u for the tile's f range, 32 values (4 x 16 bytes) per chunk; the next
-        // chunk's loads are issued before the current chunk is computed, so only the first
-        // chunk's DRAM latency is exposed
-        const uint4* grow = reinterpret_cast<const uint4*>(a.in0 + row * 2 * a.F + t.n * kBN2);
-        const uint4* urow = reinterpret_cast<const uint4*>(a.in0 + row * 2 * a.F + a.F + t.n * kBN2);
-        const int32_t nchunks = min(kBN2, a.F - t.n * kBN2) / 32;  // chunks inside F (F % 64 == 0)
-        uint4 gc[4], uc[4], gn[4], un[4];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            gc[v] = __ldg(grow + v);
-            uc[v] = __ldg(urow + v);
-        }
+        const int64_t pitch = 2 * static_cast<int64_t>(a.F) * 2;  // bytes per GU / DGU row
+        const char* gu_warp = reinterpret_cast<const char*>(a.in0 + (row - lane) * 2 * a.F);
         float partial = 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < kBN2 / 32; ++c) {
+        for (int cp = 0; cp < kBN2 / 64; ++cp) {
+            const int32_t f0 = t.n * kBN2 + cp * 64;
+            if (f0 >= a.F) break;  // warp-uniform
+            uint32_t gw[32], uw[32];
+            warp_load_row_segments(stage, gu_warp + 2 * f0, pitch, gw);
+            warp_load_row_segments(stage, gu_warp + 2 * (a.F + f0), pitch, uw);
             __syncwarp();
-            uint32_t q[32];
-            tmem_ld_32cols(taddr + c * 32, q);
-            if (c + 1 < nchunks) {
+            uint32_t q0[32], q1[32];
+            tmem_ld_32cols(taddr + cp * 64, q0);
+            tmem_ld_32cols(taddr + cp * 64 + 32, q1);
+            tmem_ld_wait(q0);
+            tmem_ld_tie(q1);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    gn[v] = __ldg(grow + 4 * (c + 1) + v);
-                    un[v] = __ldg(urow + 4 * (c + 1) + v);
+            for (int j = 0; j < 32; ++j) {  // elements 2j and 2j + 1; dg, du overwrite g, u in place
+                float dg2[2], du2[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int e = 2 * j + h;
+                    const float gg = __uint_as_float(h ? (gw[j] & 0xffff0000u) : (gw[j] << 16));
+                    const float uu = __uint_as_float(h ? (uw[j] & 0xffff0000u) : (uw[j] << 16));
+                    const float qv = __uint_as_float(e < 32 ? q0[e] : q1[e - 32]);
+                    float sig;
+                    const float act = silu_of(gg, &sig);
+                    partial += qv * act * uu;
+                    const float dh = s * qv;
+                    dg2[h] = dh * uu * sig * (1.0f + gg * (1.0f - sig));
+                    du2[h] = dh * act;
                 }
+                gw[j] = pack_bf16x2(dg2[0], dg2[1]);
+                uw[j] = pack_bf16x2(du2[0], du2[1]);
             }
-            tmem_ld_wait(q);
-            if (c < nchunks) {
-                const int32_t f0 = t.n * kBN2 + c * 32;
-                uint32_t wdg[16], wdu[16];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    float gg[8], uu[8];
-                    unpack_bf16x8(gc[v], gg);
-                    unpack_bf16x8(uc[v], uu);
-#pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        float dg2[2], du2[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const float qv = __uint_as_float(q[8 * v + i + h]);
-                            float sig;
-                            const float act = silu_of(gg[i + h], &sig);
-                            partial += qv * act * uu[i + h];
-                            const float dh = s * qv;
-                            dg2[h] = dh * uu[i + h] * sig * (1.0f + gg[i + h] * (1.0f - sig));
-                            du2[h] = dh * act;
-                        }
-                        wdg[4 * v + i / 2] = pack_bf16x2(dg2[0], dg2[1]);
-                        wdu[4 * v + i / 2] = pack_bf16x2(du2[0], du2[1]);
-                    }
-                }
-                store_64B(a.out0 + row * 2 * a.F + f0, wdg);
-                store_64B(a.out0 + row * 2 * a.F + a.F + f0, wdu);
-            }
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                gc[v] = gn[v];
-                uc[v] = un[v];
-            }
+            warp_store_row_segments(stage, gw, reinterpret_cast<char*>(a.out0 + row * 2 * a.F + f0), true);
+            warp_store_row_segments(stage, uw, reinterpret_cast<char*>(a.out0 + row * 2 * a.F + a.F + f0), true);
         }
         a.fout[row * ntn(a) + t.n] = partial;
     }
@@ -329,21 +326,24 @@ struct BwdDgradGateUp {
             tma_load_2d(sb + j * kMnBoxBytes, tb, bar, t.n * kBN2 + 64 * j, t.e * 2 * a.F + kb * kBK);
     }
 
-    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4*, const GemmArgs& a) {
+    // DXP rows leave through the staging buffer in 64-column groups (D % 64 == 0).
+    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4* stage, const GemmArgs& a) {
         const int64_t row = static_cast<int64_t>(t.row0) + row_in_tile;
 #pragma unroll 1
-        for (int c = 0; c < kBN2 / 32; ++c) {
-            __syncwarp();
-            uint32_t v[32];
-            tmem_ld_32cols(taddr + c * 32, v);
-            tmem_ld_wait(v);
-            const int32_t d0 = t.n * kBN2 + c * 32;
-            if (d0 < a.D) {
-                uint32_t w[16];
+        for (int cp = 0; cp < kBN2 / 64; ++cp) {
+            uint32_t w[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                store_64B(a.out0 + row * a.D + d0, w);
+            for (int half = 0; half < 2; ++half) {
+                __syncwarp();
+                uint32_t v[32];
+                tmem_ld_32cols(taddr + (2 * cp + half) * 32, v);
+                tmem_ld_wait(v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    w[16 * half + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
             }
+            const int32_t d0 = t.n * kBN2 + cp * 64;
+            warp_store_row_segments(stage, w, reinterpret_cast<char*>(a.out0 + row * a.D + d0), d0 < a.D);
         }
     }
 };

@@ -239,6 +239,32 @@ __device__ __forceinline__ void warp_store_row_segments(uint4* stage, const uint
     __syncwarp();
 }
 
+// The inverse: reads, for every lane of the warp, 64 bf16 (128 bytes) of that lane's own row, where
+// row i of the warp starts at base + i * row_stride bytes (16-byte aligned). Lane l loads 16-byte
+// piece (l & 7) of rows 4 j + l / 8 (j = 0..7), so each load instruction covers four whole 128-byte
+// row segments; the pieces meet in the staging rows and each lane takes its own row back as 32
+// packed words.
+__device__ __forceinline__ void warp_load_row_segments(uint4* stage, const char* base, int64_t row_stride,
+                                                       uint32_t (&words)[32]) {
+    const int lane = threadIdx.x & 31;
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        v[j] = __ldg(reinterpret_cast<const uint4*>(base + (4 * j + (lane >> 3)) * row_stride) + (lane & 7));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) stage[(4 * j + (lane >> 3)) * kStageRowU4 + (lane & 7)] = v[j];
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 x = stage[lane * kStageRowU4 + c];
+        words[4 * c] = x.x;
+        words[4 * c + 1] = x.y;
+        words[4 * c + 2] = x.z;
+        words[4 * c + 3] = x.w;
+    }
+    __syncwarp();
+}
+
 // 16 packed words (32 bf16 = 64 bytes) to a 16-byte-aligned address.
 __device__ __forceinline__ void store_64B(void* dst, const uint32_t (&w)[16]) {
     uint4* d = reinterpret_cast<uint4*>(dst);

@@ -6,7 +6,10 @@ row gather), the gate/up grouped GEMM with SwiGLU, the down grouped GEMM with th
 weighting, and the combine -- through the C ABI, on inputs already resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
-                    [--precision bf16|mxfp8|nvfp4] [--pass fwd|bwd]
+                    [--precision bf16|mxfp8|nvfp4] [--pass fwd|bwd] [--pipeline staged|mega]
+
+--pipeline mega runs the bf16 forward with both grouped GEMMs fused into one cooperative grid
+(dispatch, fused GEMMs, combine); the default runs them as separate kernels.
 
 --precision mxfp8 / nvfp4 runs a block-scaled forward (E4M3 operands with UE8M0 scales per 32, or
 E2M1 with UE4M3 scales per 16 and tensor scales; weights prepared once before the timed region,
@@ -44,6 +47,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 STAGES = ("dispatch", "gemm1_swiglu", "gemm2_score", "combine")
 KERNELS_PER_STEP = 7  # hist, scan, permute, gather, gemm1, gemm2, combine
+MEGA_STAGES = ("dispatch", "fused_gemms", "combine")
+MEGA_KERNELS_PER_STEP = 6  # hist, scan, permute, gather, the fused GEMMs, combine
 
 # Operand formats of the forward: bytes per quantized element (codes + scales), the tensor peak as
 # a multiple of the measured bf16 peak (nominal dense ratios: fp8 4.5 / 2.25, fp4 13.5 / 2.25), the
@@ -69,6 +74,8 @@ def parse_args(argv=None):
                    help="forward operands: bf16, MXFP8 E4M3 or NVFP4 E2M1 (block-scaled, prepared weights)")
     p.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
                    help="fwd: the forward layer (the headline); bwd: its backward pass (one call per step)")
+    p.add_argument("--pipeline", default="staged", choices=["staged", "mega"],
+                   help="bf16 forward: separate GEMM kernels (staged) or both GEMMs in one grid (mega)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--tokens", type=int, default=None,
                    help="replace the workload's T (smaller cases for profiling runs)")
@@ -144,6 +151,8 @@ def kernel_costs(T, D, F, E, K, touched, q=None):
         "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + 2 * R * D * 2},
         "gemm1_swiglu": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * 2 + R * D * 2 + R * F * 2},
         "gemm2_score": {"flops": 2 * R * D * F, "bytes": touched * D * F * 2 + R * F * 2 + R * D * 2 + R * 8},
+        # both GEMMs in one grid: H stays inside the kernel, so only XP in and Y out count
+        "fused_gemms": {"flops": 6 * R * D * F, "bytes": touched * 3 * F * D * 2 + R * D * 2 + R * D * 2 + R * 8},
         "combine": {"flops": 0, "bytes": R * D * 2 + T * D * 2 + R * 4},
     }
 
@@ -382,6 +391,10 @@ def run_ours(args, rank, world, local_rank):
     prec = PRECISIONS[args.precision]
     mx = args.precision == "mxfp8"
     nv = args.precision == "nvfp4"
+    mega = args.pipeline == "mega"
+    if mega and (mx or nv):
+        raise SystemExit("--pipeline mega runs the bf16 forward")
+    stages = MEGA_STAGES if mega else STAGES
     gx = 0.0
     if mx:  # prepared once, as the pages prepare block-scaled weights before execution
         w13_mx = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W13, w13)
@@ -392,6 +405,8 @@ def run_ours(args, rank, world, local_rank):
         w2_nv = binding.moe_nvfp4_prepare_weight(binding.MOE_WEIGHT_W2, w2)
         gx = float(torch.tensor(x.abs().max().float().item(), dtype=torch.float32) / 2688.0)
         ws = binding.alloc_workspace(binding.moe_nvfp4_workspace_bytes(*dims), device)
+    elif mega:
+        ws = binding.alloc_workspace(binding.moe_mega_workspace_bytes(*dims), device)
     else:
         ws = binding.alloc_workspace(binding.moe_workspace_bytes(*dims), device)
     out = torch.empty((T, D), dtype=torch.bfloat16, device=device)
@@ -410,6 +425,14 @@ def run_ours(args, rank, world, local_rank):
                                                  s + 1, stream)
             if ev is not None:
                 ev[binding.MX_STAGES].record(stream)
+            return
+        if mega:
+            for s in range(binding.MEGA_STAGES):
+                if ev is not None:
+                    ev[s].record(stream)
+                binding.moe_fwd_mega_stages(x, ids, scores, w13, w2, out, ws, s, s + 1, stream)
+            if ev is not None:
+                ev[binding.MEGA_STAGES].record(stream)
             return
         if ev is not None:
             ev[0].record(stream)
@@ -434,12 +457,13 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status bits {status:#x} after warm-up")
     counts = (binding.moe_mxfp8_workspace_layout(*dims) if mx else
-              binding.moe_nvfp4_workspace_layout(*dims) if nv else binding.moe_workspace_layout(*dims))
+              binding.moe_nvfp4_workspace_layout(*dims) if nv else
+              binding.moe_mega_workspace_layout(*dims) if mega else binding.moe_workspace_layout(*dims))
     cnt = ws[counts["counts"]:counts["counts"] + 4 * E].view(torch.int32)
     touched = int((cnt > 0).sum().item())
 
     # ------------------------------------------------------------------ device-timed region
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid) if hasattr(
         torch.cuda.get_device_properties(device), "uuid") else str(local_rank)
     sampler = ClockSampler(gpu_id)
@@ -455,8 +479,8 @@ def run_ours(args, rank, world, local_rank):
     barrier(dist, device)
     sampler.stop()
     stage_ms = {s: [events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps)]
-                for j, s in enumerate(STAGES)}
-    step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(args.steps)]
+                for j, s in enumerate(stages)}
+    step_ms = [events[i][0].elapsed_time(events[i][len(stages)]) for i in range(args.steps)]
     total_s = reduce_max(dist, sum(step_ms) / 1e3)
 
     # ------------------------------------------------------------------ end to end (host buffers)
@@ -501,6 +525,8 @@ def run_ours(args, rank, world, local_rank):
             elif nv:
                 binding.moe_routed_experts_fwd_nvfp4(x_d[b], ids_d[b], scores_d[b], w13_nv, w2_nv, out_d[b], ws,
                                                      (F, E), gx, NV_H_SCALE, stream)
+            elif mega:
+                binding.moe_routed_experts_fwd_mega(x_d[b], ids_d[b], scores_d[b], w13, w2, out_d[b], ws, stream)
             else:
                 binding.moe_routed_experts_fwd(x_d[b], ids_d[b], scores_d[b], w13, w2, out_d[b], ws, stream)
             computed[b].record(stream)
@@ -566,7 +592,7 @@ def run_ours(args, rank, world, local_rank):
         dtype=prec["dtype"],
         data="synthetic",
         config={"workload": args.config if not args.tokens else f"{args.config} (T={T})", "T": T, "D": D, "F": F,
-                "precision": args.precision,
+                "precision": args.precision, "pipeline": args.pipeline,
                 "E": E, "K": K, "routing": wl.routing, "experts_touched": touched, "global_batch": T * world, "parallelism": f"replicas{world}",
                 "l2": "flushed between steps (512 MB write)", "seed": args.seed},
         tflops=round(world * flops / step_s / 1e12, 2),
@@ -576,7 +602,7 @@ def run_ours(args, rank, world, local_rank):
         stage_ms={s: round(v, 4) for s, v in mean_stage.items()},
         e2e={"value": round(world * T * args.steps / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
              "d2h_bytes_per_step": d2h},
-        gpu_launches=KERNELS_PER_STEP * args.steps,
+        gpu_launches=(MEGA_KERNELS_PER_STEP if mega else KERNELS_PER_STEP) * args.steps,
         clocks=sampler.summary(),
         wall_s=round(wall, 3),
         cpu_baseline=cpu,
@@ -709,7 +735,7 @@ def run_reference(args, rank, world, local_rank):
         warmup=args.warmup, ms_per_step=round(total * 1e3 / args.steps, 3), higher_is_better=True,
         scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
         config={"workload": args.config, "T": T, "D": D, "F": F, "E": E, "K": K, "routing": wl.routing,
-                "precision": args.precision, "sample_tokens": n_tok},
+                "precision": args.precision, "pipeline": args.pipeline, "sample_tokens": n_tok},
         cpu_baseline={"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
         e2e={"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     ), flush=True)

@@ -84,8 +84,12 @@ enum {
                                 outputs per pair                                              */
     MOE_WS_H = 10,           /* bf16 [T*K, F] SwiGLU output per routed row                     */
     MOE_WS_RMS = 11,         /* fp32 [T*K, ceil(D/256)] per-tile sums of squares (RMSNorm mode) */
-    MOE_WS_TOTAL = 12,       /* total bytes (== moe_workspace_bytes)                          */
-    MOE_WS_REGIONS = 13
+    MOE_WS_READY = 12,       /* fused forward only: uint32 [32 + ceil(T*K/128) + min(T*K, E)], the
+                                fused grid's tile counter and its row-tile readiness counters */
+    MOE_WS_Y = 13,           /* fused forward only: bf16 [T, K, D] score-weighted pair outputs  */
+    MOE_WS_TOTAL = 14,       /* total bytes (== moe_workspace_bytes, or moe_mega_workspace_bytes
+                                in the fused layout)                                          */
+    MOE_WS_REGIONS = 15
 };
 
 /*
@@ -101,6 +105,15 @@ size_t moe_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K
  */
 moe_status_t moe_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
                                   size_t *region_offsets);
+
+/*
+ * Bytes of device workspace that moe_routed_experts_fwd_mega needs, and its region offsets: the
+ * layout above with the READY and Y regions filled in (both are empty in the staged layout).
+ * Pure arithmetic; 0 / MOE_ERR_* for sizes outside the shape limits.
+ */
+size_t moe_mega_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K);
+moe_status_t moe_mega_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                       size_t *region_offsets);
 
 /*
  * Bytes of device workspace that moe_routing needs (status word and per-block scratch).
@@ -164,6 +177,48 @@ moe_status_t moe_routed_experts_fwd_rmsnorm(const void *x, const int32_t *topk_i
                                             int32_t scores_dtype, const void *w13, const void *w2, void *out,
                                             int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, float eps,
                                             void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * The forward pass with the two grouped GEMMs fused into one pipeline (Dist-MoE 0.1.0,
+ * "Block-scaled execution": the Mega pipeline runs both projections as one chunked pipeline, with
+ * the staged pipeline's tensor and memory contracts). One cooperative grid walks the gate/up
+ * tiles of expert e and the down tiles of an earlier expert in turn; a down tile starts once the
+ * gate/up tiles of its 128 rows have written their H rows, so H is read back from L2 and the two
+ * GEMMs share one launch and one tail. The tiles and roundings are those of
+ * moe_routed_experts_fwd: the output is bit-identical to it.
+ *
+ * Arguments as for moe_routed_experts_fwd, except
+ *   workspace    device, moe_mega_workspace_bytes(T, D, F, E, K) bytes (it adds the READY
+ *                counters and a Y region that may not overlap XP, because Y rows are written
+ *                while later experts' XP rows are still being read)
+ * Errors as for moe_routed_experts_fwd; MOE_ERR_CUDA also when the device cannot hold the grid
+ * as one cooperative launch (never on a whole GB300). A row tile whose H never arrives ends the
+ * kernel through its bounded wait with MOE_DEV_TIMEOUT.
+ */
+moe_status_t moe_routed_experts_fwd_mega(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                         int32_t scores_dtype, const void *w13, const void *w2, void *out,
+                                         int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                         void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Stages of the fused forward, for moe_fwd_mega_stages. */
+enum {
+    MOE_MEGA_STAGE_DISPATCH = 0, /* status word cleared, routing, x rows gathered (XP)             */
+    MOE_MEGA_STAGE_GEMMS = 1,    /* readiness counters cleared; both grouped GEMMs in one grid (H, Y) */
+    MOE_MEGA_STAGE_COMBINE = 2,  /* out from Y                                                      */
+    MOE_MEGA_STAGES = 3
+};
+
+/*
+ * Stages stage_begin .. stage_end-1 of moe_routed_experts_fwd_mega (0 <= stage_begin <= stage_end
+ * <= MOE_MEGA_STAGES; the full range is that call), each needing the previous stages' workspace
+ * contents. Arguments as for moe_routed_experts_fwd_mega; an out-of-range stage pair returns
+ * MOE_ERR_INVALID_ARG before any launch.
+ */
+moe_status_t moe_fwd_mega_stages(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                                 int32_t scores_dtype, const void *w13, const void *w2, void *out, int64_t T,
+                                 int32_t D, int32_t F, int32_t E, int32_t K, int32_t stage_begin,
+                                 int32_t stage_end, void *workspace, size_t workspace_bytes,
+                                 moe_stream_t stream);
 
 /*
  * Stage 1 of the forward pass: clears the status word, routes the pairs into the workspace's

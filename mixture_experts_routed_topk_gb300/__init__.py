@@ -16,6 +16,10 @@ __all__ = [
     "moe_fwd_combine",
     "moe_routed_experts_fwd",
     "moe_routed_experts_fwd_rmsnorm",
+    "moe_mega_workspace_bytes",
+    "moe_mega_workspace_layout",
+    "moe_routed_experts_fwd_mega",
+    "moe_fwd_mega_stages",
     "moe_bwd_workspace_bytes",
     "moe_routed_experts_bwd",
     "moe_mxfp8_weight_bytes",

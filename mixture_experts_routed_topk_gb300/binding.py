@@ -25,7 +25,7 @@ MOE_DEV_TIMEOUT = 2
 
 WS_REGIONS = (
     "status", "counts", "offsets", "tiles1", "tiles2", "block_counts", "block_bases",
-    "perm", "inv", "xp", "h", "rms", "total",
+    "perm", "inv", "xp", "h", "rms", "ready", "y", "total",
 )
 MOE_WEIGHT_W13 = 0
 MOE_WEIGHT_W2 = 1
@@ -68,6 +68,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "moe_routing": ([vp, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "moe_routed_experts_fwd": (
                 [vp, vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_mega_workspace_bytes": ([i64, i32, i32, i32, i32], sz),
+            "moe_mega_workspace_layout": ([i64, i32, i32, i32, i32, vp], ctypes.c_int),
+            "moe_routed_experts_fwd_mega": (
+                [vp, vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_fwd_mega_stages": (
+                [vp, vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
             "moe_routed_experts_fwd_rmsnorm": (
                 [vp, vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, ctypes.c_float, vp, sz, vp], ctypes.c_int),
             "moe_fwd_dispatch": ([vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
@@ -164,6 +170,17 @@ def moe_workspace_layout(T: int, D: int, F: int, E: int, K: int) -> dict:
     return dict(zip(WS_REGIONS, (int(v) for v in arr)))
 
 
+def moe_mega_workspace_bytes(T: int, D: int, F: int, E: int, K: int) -> int:
+    return int(load().moe_mega_workspace_bytes(T, D, F, E, K))
+
+
+def moe_mega_workspace_layout(T: int, D: int, F: int, E: int, K: int) -> dict:
+    arr = (ctypes.c_size_t * len(WS_REGIONS))()
+    _check("moe_mega_workspace_layout",
+           load().moe_mega_workspace_layout(T, D, F, E, K, ctypes.cast(arr, ctypes.c_void_p)))
+    return dict(zip(WS_REGIONS, (int(v) for v in arr)))
+
+
 def moe_routing_workspace_bytes(T: int, E: int, K: int) -> int:
     return int(load().moe_routing_workspace_bytes(T, E, K))
 
@@ -201,6 +218,45 @@ def moe_routed_experts_fwd(x, topk_ids, topk_scores, w13, w2, out, workspace, st
     _check("moe_routed_experts_fwd", load().moe_routed_experts_fwd(
         _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(out),
         T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_routed_experts_fwd_mega(x, topk_ids, topk_scores, w13, w2, out, workspace, stream=None) -> None:
+    """The forward pass with both grouped GEMMs in one fused pipeline; the workspace is
+    moe_mega_workspace_bytes(T, D, F, E, K) bytes. Bit-identical to moe_routed_experts_fwd."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
+    _need(w13, "w13", torch.bfloat16, 4)
+    _need(w2, "w2", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 2)
+    _need(workspace, "workspace", torch.uint8)
+    T, D, F, E, K = _dims(x, topk_ids, w13)
+    if tuple(w2.shape) != (E, D, F) or tuple(out.shape) != (T, D) or tuple(topk_scores.shape) != (T, K):
+        raise ValueError("inconsistent shapes among w2 [E,D,F], out [T,D], topk_scores [T,K]")
+    sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
+    _check("moe_routed_experts_fwd_mega", load().moe_routed_experts_fwd_mega(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(out),
+        T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+MEGA_STAGES = 3  # dispatch, both GEMMs in one grid, combine
+
+
+def moe_fwd_mega_stages(x, topk_ids, topk_scores, w13, w2, out, workspace, stage_begin: int, stage_end: int,
+                        stream=None) -> None:
+    """Stages [stage_begin, stage_end) of moe_routed_experts_fwd_mega (MEGA_STAGES in all)."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
+    _need(w13, "w13", torch.bfloat16, 4)
+    _need(w2, "w2", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 2)
+    _need(workspace, "workspace", torch.uint8)
+    T, D, F, E, K = _dims(x, topk_ids, w13)
+    sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
+    _check("moe_fwd_mega_stages", load().moe_fwd_mega_stages(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(out),
+        T, D, F, E, K, int(stage_begin), int(stage_end), _ptr(workspace), workspace.numel(), _stream_handle(stream)))
 
 
 def moe_routed_experts_fwd_rmsnorm(x, topk_ids, topk_scores, w13, w2, out, workspace, eps: float = 1e-6,

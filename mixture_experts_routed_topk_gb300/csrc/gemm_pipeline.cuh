@@ -30,7 +30,20 @@
 //        (block-scaled shapes: load(t, kb, sa, sb, sf, bar, ta, tb, args), sf = the scale chunks)
 //   __device__ static void epilogue(const Tile&, uint32_t taddr, int row, uint4* stage,
 //                                   const GemmArgs&)          (taddr = this warp's TMEM lanes)
-// Every load() must deliver exactly the shape's kTxBytes into the stage.
+// Every load() must deliver exactly the shape's kTxBytes into the stage. ta and tb point into the
+// kernel's array of four tensor maps (tb == ta + 1); a policy with more operands reads ta[2], ta[3].
+// Optional:
+//   __device__ static bool acquire(const Tile&, const GemmArgs&, volatile int* abort)
+//        run by the producer before a tile's first load: waits (bounded) until data that other
+//        CTAs of the same grid produce for this tile is visible to TMA; false aborts the CTA.
+//   static constexpr bool kCooperative = true
+//        launch as a cooperative grid (every CTA resident at once), required when acquire()
+//        waits for tiles other CTAs own.
+//   static constexpr bool kDynamicSchedule = true
+//        CTAs take tiles in list order from the global counter args.ticket (zero on entry)
+//        instead of the fixed c, c + grid, ...: the producer takes a tile and hands its index to
+//        the MMA and epilogue warps through a small ring of shared-memory slots. For tile lists of
+//        unequal tiles, where a fixed assignment lets CTAs drift apart along the list.
 #pragma once
 
 #include <cuda.h>
@@ -39,6 +52,7 @@
 
 #include <atomic>
 #include <type_traits>
+#include <utility>
 
 #include "moe_internal.cuh"
 #include "ptx_sm103.cuh"
@@ -110,6 +124,13 @@ static_assert(Nvf4Shape::kStageBytes % 1024 == 0 && Nvf4Shape::kStages == 5, "st
 static_assert(Mxf8Shape::kStageBytes % 1024 == 0 && Mxf8Shape::kTxBytes <= Mxf8Shape::kStageBytes, "stage");
 static_assert(Mxf8Shape::kStages == 4 && kMxBN + 64 == Mxf8Shape::kAccCols, "four 32-column scale slots in the gaps");
 
+// The kernel's tensor maps: A and B of the policy's GEMM, then two more for policies that run
+// two GEMMs in one grid. Passed as one __grid_constant__ parameter, so TMA reads them from the
+// parameter space.
+struct GemmMaps {
+    CUtensorMap m[4];
+};
+
 template <class P, class = void>
 struct ShapeOf {
     using type = Bf16Shape;
@@ -127,12 +148,19 @@ constexpr int kMnBoxBytes = 64 * kBK * 2;   // one 64 (M or N) x 64 (K) MN-major
 constexpr int kStageRowU4 = 9;  // 144-byte row stride in 16-byte units
 constexpr int kEpilogueStagingBytes = (kEpilogueThreads / 32) * 32 * kStageRowU4 * 16;
 
+constexpr int kTileRing = 4;  // tiles in flight between producer and consumers (dynamic schedule)
+constexpr int kTileStoreBytes = 32;
+
 struct alignas(8) PipeState {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t tile_full[kTileRing];   // producer -> MMA + epilogue: a tile is in the slot
+    uint64_t tile_empty[kTileRing];  // MMA + 4 epilogue warps -> producer: the slot was read
+    uint32_t tile_ring[kTileRing];   // the tile's index in the list (>= the tile count: no more tiles)
+    alignas(16) uint8_t tile_store[kTileRing][kTileStoreBytes];  // the producer's decode of it
     uint32_t tmem_base;
     int abort;
 };
@@ -171,9 +199,33 @@ struct GemmArgs {
     uint8_t* q_out;          // E4M3 output codes
     uint8_t* sf_out;         // the output's scale chunks
     int32_t ntn;             // column tiles per row tile
+    // two-GEMM grids (the fused forward): the second GEMM's tile prefix, K steps and column tiles,
+    // and one readiness counter per row tile, counting first-GEMM epilogue warps that finished
+    const int32_t* tiles_b;
+    int32_t kblocks_b;
+    int32_t ntn_b;
+    uint32_t* ready;
+    uint32_t* ticket;        // dynamic schedule: the next unclaimed tile of the list
     float act_scale_a;       // NVFP4: tensor scale of the A operand's activations
     float act_scale_out;     // NVFP4: tensor scale used to quantize the epilogue's output
 };
+
+template <class P, class = void>
+struct HasAcquire : std::false_type {};
+template <class P>
+struct HasAcquire<P, std::void_t<decltype(P::acquire(std::declval<const typename P::Tile&>(),
+                                                       std::declval<const GemmArgs&>(),
+                                                       std::declval<volatile int*>()))>> : std::true_type {};
+
+template <class P, class = void>
+struct IsDynamic : std::false_type {};
+template <class P>
+struct IsDynamic<P, std::void_t<decltype(P::kDynamicSchedule)>> : std::integral_constant<bool, P::kDynamicSchedule> {};
+
+template <class P, class = void>
+struct IsCooperative : std::false_type {};
+template <class P>
+struct IsCooperative<P, std::void_t<decltype(P::kCooperative)>> : std::integral_constant<bool, P::kCooperative> {};
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -282,9 +334,10 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 
 template <class P>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    k_grouped_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   const GemmArgs args) {
+    k_grouped_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
     using S = typename ShapeOf<P>::type;
+    const CUtensorMap* tmap_a = &maps.m[0];
+    const CUtensorMap* tmap_b = &maps.m[1];
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must start on 1024-byte boundaries of the shared address space
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
@@ -306,10 +359,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&ps->acc_empty[b], kEpilogueThreads);
         }
         mbar_init(&ps->drain, 1);
+        for (int r = 0; r < kTileRing; ++r) {
+            mbar_init(&ps->tile_full[r], 1);
+            mbar_init(&ps->tile_empty[r], 1 + kEpilogueThreads / 32);
+        }
         ps->abort = 0;
         mbar_init_fence();
-        tma_prefetch_descriptor(&tmap_a);
-        tma_prefetch_descriptor(&tmap_b);
+        tma_prefetch_descriptor(tmap_a);
+        tma_prefetch_descriptor(tmap_b);
+        if constexpr (HasAcquire<P>::value) {
+            tma_prefetch_descriptor(&maps.m[2]);
+            tma_prefetch_descriptor(&maps.m[3]);
+        }
     }
     if (warp == 1) {
         __syncwarp();
@@ -324,14 +385,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     griddep_launch_dependents();
     const uint32_t tmem_base = ps->tmem_base;
     const int32_t total = P::num_tiles(args);
+    constexpr bool kDynamic = IsDynamic<P>::value;
+    static_assert(!kDynamic || (sizeof(typename P::Tile) <= kTileStoreBytes &&
+                                std::is_trivially_copyable<typename P::Tile>::value),
+                  "a dynamically scheduled policy's tiles travel through the shared-memory ring");
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int32_t tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const typename P::Tile t = P::decode(tile, args);
+            // tile indices are compared unsigned: the list has fewer than 2^31 tiles, and the end
+            // marks and the last claimed tickets lie at most a few grids past its end
+            const uint32_t utotal = static_cast<uint32_t>(total);
+            // The next tile is claimed and decoded one tile ahead, right after the current tile's
+            // first stage is issued, so neither the claim nor the decode delays the first loads of
+            // a tile (the stage ring covers them).
+            uint32_t tile = kDynamic ? atomicAdd(args.ticket, 1u) : blockIdx.x;
+            typename P::Tile t{};
+            if (tile < utotal) t = P::decode(static_cast<int32_t>(tile), args);
+            for (uint32_t i = 0; ok; ++i) {
+                uint32_t next;
+                if constexpr (kDynamic) {
+                    // hand the tile, decoded (or the end mark, any index >= total), to the MMA and
+                    // epilogue warps
+                    const uint32_t r = i % kTileRing, rph = (i / kTileRing) & 1u;
+                    if (!mbar_wait(&ps->tile_empty[r], rph ^ 1u, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    ps->tile_ring[r] = tile;
+                    *reinterpret_cast<typename P::Tile*>(ps->tile_store[r]) = t;
+                    mbar_arrive(&ps->tile_full[r]);
+                    if (tile >= utotal) break;
+                    next = atomicAdd(args.ticket, 1u);  // its value is first needed after stage 0
+                } else {
+                    if (tile >= utotal) break;
+                    next = tile + gridDim.x;
+                }
+                if constexpr (HasAcquire<P>::value) {
+                    if (!P::acquire(t, args, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                typename P::Tile nt{};
+                bool decoded = false;
                 for (int32_t kb = 0; kb < t.kblocks; ++kb, ++it) {
                     const uint32_t s = it % S::kStages;
                     const uint32_t ph = (it / S::kStages) & 1u;
@@ -342,11 +441,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint8_t* sa = smem + s * S::kStageBytes;
                     mbar_arrive_expect_tx(&ps->full[s], S::kTxBytes);
                     if constexpr (S::kBlockScaled)
-                        P::load(t, kb, sa, sa + S::kABytes, sa + S::kABytes + S::kBBytes, &ps->full[s], &tmap_a,
-                                &tmap_b, args);
+                        P::load(t, kb, sa, sa + S::kABytes, sa + S::kABytes + S::kBBytes, &ps->full[s], tmap_a,
+                                tmap_b, args);
                     else
-                        P::load(t, kb, sa, sa + S::kABytes, &ps->full[s], &tmap_a, &tmap_b, args);
+                        P::load(t, kb, sa, sa + S::kABytes, &ps->full[s], tmap_a, tmap_b, args);
+                    if (!decoded) {
+                        if (next < utotal) nt = P::decode(static_cast<int32_t>(next), args);
+                        decoded = true;
+                    }
                 }
+                if (!ok) break;
+                if (!decoded && next < utotal) nt = P::decode(static_cast<int32_t>(next), args);
+                tile = next;
+                t = nt;
             }
             if (!ok) {
                 // aborting: give the copies already issued time to land before the CTA exits
@@ -358,10 +465,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, tcount = 0;
+            uint32_t it = 0;
             bool ok = true;
-            for (int32_t tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tcount) {
-                const typename P::Tile t = P::decode(tile, args);
+            // static schedule: each tile is decoded during the previous one (after its first MMAs
+            // are issued), so the decode never leaves the tensor pipe idle between tiles
+            typename P::Tile t{}, nt{};
+            if (!kDynamic && blockIdx.x < static_cast<uint32_t>(total)) nt = P::decode(static_cast<int32_t>(blockIdx.x), args);
+            for (uint32_t tcount = 0; ok; ++tcount) {
+                uint32_t tile;
+                if constexpr (kDynamic) {
+                    const uint32_t r = tcount % kTileRing, rph = (tcount / kTileRing) & 1u;
+                    if (!mbar_wait(&ps->tile_full[r], rph, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tile = ps->tile_ring[r];
+                    t = *reinterpret_cast<const typename P::Tile*>(ps->tile_store[r]);
+                    mbar_arrive(&ps->tile_empty[r]);
+                } else {
+                    tile = blockIdx.x + tcount * gridDim.x;
+                    t = nt;  // decoded during the previous tile
+                }
+                if (tile >= static_cast<uint32_t>(total)) break;
+                const uint32_t next = tile + gridDim.x;  // static schedule only
+                bool decoded = kDynamic;
                 const uint32_t acc = tcount & 1u;
                 const uint32_t aph = (tcount >> 1) & 1u;
                 if (!mbar_wait(&ps->acc_empty[acc], aph ^ 1u, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
@@ -402,8 +529,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                         operand_desc<P::kBMnMajor>(b0, kk), P::kIdesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit(&ps->empty[s]);  // frees the stage once these MMAs have read it
+                    if (!decoded) {
+                        if (next < static_cast<uint32_t>(total)) nt = P::decode(static_cast<int32_t>(next), args);
+                        decoded = true;
+                    }
                 }
                 if (!ok) break;
+                if (!decoded && next < static_cast<uint32_t>(total)) nt = P::decode(static_cast<int32_t>(next), args);
                 mma_commit(&ps->acc_full[acc]);  // a tile without K steps signals at once
             }
             if (!ok) {
@@ -420,9 +552,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row_in_tile = quarter * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         uint4* wstage = staging + (warp - 2) * 32 * kStageRowU4;
-        uint32_t tcount = 0;
-        for (int32_t tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
-            const typename P::Tile t = P::decode(tile, args);
+        for (uint32_t tcount = 0;; ++tcount) {
+            uint32_t tile;
+            typename P::Tile t;
+            if constexpr (kDynamic) {
+                const uint32_t r = tcount % kTileRing, rph = (tcount / kTileRing) & 1u;
+                if (!warp_wait(&ps->tile_full[r], rph, abort_flag, args.status)) break;
+                __syncwarp();  // orders every lane's reads of the slot after lane 0's wait
+                tile = ps->tile_ring[r];
+                t = *reinterpret_cast<const typename P::Tile*>(ps->tile_store[r]);
+                __syncwarp();  // every lane has read the slot
+                if (lane == 0) mbar_arrive(&ps->tile_empty[r]);
+                if (tile >= static_cast<uint32_t>(total)) break;
+            } else {
+                tile = blockIdx.x + tcount * gridDim.x;
+                if (tile >= static_cast<uint32_t>(total)) break;
+                t = P::decode(static_cast<int32_t>(tile), args);
+            }
             const uint32_t acc = tcount & 1u;
             const uint32_t aph = (tcount >> 1) & 1u;
             if (!warp_wait(&ps->acc_full[acc], aph, abort_flag, args.status)) break;
@@ -456,8 +602,7 @@ bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t r
 int sm_count_grid(int64_t max_tiles, int sm_count);
 
 template <class P>
-moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                         cudaStream_t stream) {
+moe_status_t launch_gemm(const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t stream) {
     constexpr size_t kGemmSmemBytes = gemm_smem_bytes<typename ShapeOf<P>::type>();
     constexpr int kMaxDevices = 64;
     static std::atomic<bool> attr_set[kMaxDevices];
@@ -469,10 +614,35 @@ moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gem
             return MOE_ERR_CUDA;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_grouped_gemm<P>, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, stream, ta, tb, a) ==
-                   cudaSuccess
-               ? MOE_OK
-               : MOE_ERR_CUDA;
+    if constexpr (IsCooperative<P>::value) {
+        // every CTA resident at once (one per SM at this shared-memory size), so a CTA that waits
+        // for another CTA's tile never waits for one that has not started
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kGemmThreads);
+        cfg.dynamicSmemBytes = kGemmSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, k_grouped_gemm<P>, maps, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    } else {
+        return launch_pdl(k_grouped_gemm<P>, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, stream, maps, a) ==
+                       cudaSuccess
+                   ? MOE_OK
+                   : MOE_ERR_CUDA;
+    }
+}
+
+template <class P>
+moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
+                         cudaStream_t stream) {
+    GemmMaps maps{};
+    maps.m[0] = ta;
+    maps.m[1] = tb;
+    return launch_gemm<P>(maps, a, grid, stream);
 }
 
 }  // namespace moe

@@ -108,6 +108,12 @@ struct FwdDownT {
     }
 
     __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4* stage, const GemmArgs& a) {
+        epilogue_to(t, taddr, row_in_tile, stage, a, a.out0);
+    }
+
+    // The epilogue with an explicit destination for the Y rows.
+    __device__ static void epilogue_to(const RowTile& t, uint32_t taddr, int row_in_tile, uint4* stage,
+                                       const GemmArgs& a, __nv_bfloat16* y) {
         const bool valid = row_in_tile < t.rows;
         const int64_t row = static_cast<int64_t>(t.row0) + row_in_tile;
         int32_t pair = 0;
@@ -137,10 +143,144 @@ struct FwdDownT {
             }
             const int32_t d0 = t.n * kBN2 + cp * 64;  // D % 64 == 0: the 64 columns are all in or all out
             warp_store_row_segments(stage, words,
-                                    reinterpret_cast<char*>(a.out0 + static_cast<int64_t>(pair) * a.D + d0),
+                                    reinterpret_cast<char*>(y + static_cast<int64_t>(pair) * a.D + d0),
                                     valid && d0 < a.D);
         }
         if (kRms && valid) a.fout[static_cast<int64_t>(pair) * ((a.D + kBN2 - 1) / kBN2) + t.n] = sumsq;
+    }
+};
+
+// ------------------------------------------------------------------ the fused (Mega) forward
+//
+// Both GEMMs in one cooperative grid (Dist-MoE 0.1.0, "Block-scaled execution": the Mega pipeline
+// runs the two projections as one chunked pipeline instead of separate W13 and SwiGLU/W2 kernels).
+// The grid walks one interleaved list of slots: a slot is one expert's gate/up tiles (phase 0) or
+// its down tiles (phase 1); expert e's down slot comes after the gate/up slot of expert e + L, so
+// its H rows are written about L experts earlier and are read back while still in L2:
+//     G1(0) .. G1(L-1), G1(L) G2(0), G1(L+1) G2(1), .., G1(E-1) G2(E-L-1), G2(E-L) .. G2(E-1)
+// Inside a slot the order is the staged kernels' (rows fastest). CTAs claim tiles in list order
+// from a global counter (the tiles differ in length, so a fixed assignment would let CTAs drift
+// apart along the list). A down tile's producer waits (bounded) until the four epilogue warps of
+// every gate/up tile of its row tile have released the row tile's counter; those tiles come
+// earlier in the list and were claimed by running CTAs, so the lowest unfinished tile can always
+// proceed. The tiles, their arithmetic and their roundings are
+// the staged kernels', so the result is bit-identical to the staged forward's.
+
+struct MegaTile : RowTile {
+    int32_t phase;  // 0: gate/up + SwiGLU, 1: down + score
+    int32_t rt;     // row tile index over all experts (the readiness counter)
+};
+
+// Gate/up slots (a) and down slots (b) among the first k slots of the interleaved list, lag L.
+__device__ __forceinline__ void mega_slots_before(int32_t k, int32_t E, int32_t L, int32_t& a, int32_t& b) {
+    if (k <= L) {
+        a = k;
+        b = 0;
+    } else if (k <= 2 * E - L) {
+        const int32_t j = k - L;
+        a = L + (j + 1) / 2;
+        b = j / 2;
+    } else {
+        a = E;
+        b = k - E;
+    }
+}
+
+// Lag in experts: the gate/up tiles of about two waves of the grid between an expert's gate/up
+// slot and its down slot.
+__device__ __forceinline__ int32_t mega_lag(const GemmArgs& a) {
+    // 2 * grid * E < 2^31 (grid <= SM count, E <= 4096)
+    const uint32_t g1 = max(__ldg(a.tiles + a.E), 1);
+    const uint32_t want = (2u * gridDim.x * static_cast<uint32_t>(a.E) + g1 - 1) / g1;
+    return static_cast<int32_t>(min(max(want, 1u), static_cast<uint32_t>(a.E)));
+}
+
+struct FwdMega {
+    using Tile = MegaTile;
+    static constexpr bool kAMnMajor = false, kBMnMajor = false;
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBRows);
+    static constexpr bool kCooperative = true;
+    static constexpr bool kDynamicSchedule = true;  // gate/up and down tiles differ in length
+    static_assert(FwdGateUp::kIdesc == kIdesc && FwdDownT<false>::kIdesc == kIdesc, "one accumulator shape");
+
+    __device__ static int32_t num_tiles(const GemmArgs& a) { return __ldg(a.tiles + a.E) + __ldg(a.tiles_b + a.E); }
+
+    __device__ static Tile decode(int32_t tile, const GemmArgs& a) {
+        const int32_t L = mega_lag(a);
+        // the last slot k whose first tile is <= tile
+        int32_t lo = 0, hi = 2 * a.E - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            int32_t na, nb;
+            mega_slots_before(mid, a.E, L, na, nb);
+            if (__ldg(a.tiles + na) + __ldg(a.tiles_b + nb) <= tile) lo = mid;
+            else hi = mid - 1;
+        }
+        int32_t na, nb;
+        mega_slots_before(lo, a.E, L, na, nb);
+        Tile t;
+        if (lo < L) {
+            t.phase = 0;
+            t.e = lo;
+        } else if (lo < 2 * a.E - L) {
+            const int32_t j = lo - L;
+            t.phase = j & 1;
+            t.e = (j & 1) ? (j - 1) / 2 : L + j / 2;
+        } else {
+            t.phase = 1;
+            t.e = lo - a.E;
+        }
+        const int32_t local = tile - __ldg(a.tiles + na) - __ldg(a.tiles_b + nb);
+        const int32_t ne = __ldg(a.counts + t.e);
+        const int32_t mt = (ne + kBM - 1) / kBM;
+        t.n = local / mt;
+        const int32_t m = local - t.n * mt;
+        t.row0 = __ldg(a.offsets + t.e) + m * kBM;
+        t.rows = min(kBM, ne - m * kBM);
+        t.kblocks = t.phase ? a.kblocks_b : a.kblocks;
+        t.rt = __ldg(a.tiles + t.e) / a.ntn + m;
+        return t;
+    }
+
+    // Down tiles: wait until every gate/up epilogue warp of the row tile has released its H rows.
+    __device__ static bool acquire(const Tile& t, const GemmArgs& a, volatile int* abort) {
+        if (t.phase == 0) return true;
+        const uint32_t target = 4u * static_cast<uint32_t>(a.ntn);
+        const uint32_t* flag = a.ready + t.rt;
+        if (ld_acquire_gpu(flag) < target) {
+            const unsigned long long t0 = global_timer_ns();
+            while (ld_acquire_gpu(flag) < target) {
+                if (*abort) return false;
+                if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                    atomicOr(a.status, MOE_DEV_TIMEOUT);
+                    *abort = 1;
+                    return false;
+                }
+                __nanosleep(64);
+            }
+        }
+        fence_proxy_async_global();  // the H rows are read next by TMA
+        return true;
+    }
+
+    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
+                                const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs& a) {
+        if (t.phase == 0) FwdGateUp::load(t, kb, sa, sb, bar, ta, tb, a);
+        else FwdDownT<false>::load(t, kb, sa, sb, bar, ta + 2, ta + 3, a);
+    }
+
+    __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4* stage, const GemmArgs& a) {
+        if (t.phase == 1) {
+            FwdDownT<false>::epilogue_to(t, taddr, row_in_tile, stage, a, a.out1);
+            return;
+        }
+        FwdGateUp::epilogue(t, taddr, row_in_tile, stage, a);
+        // release this warp's 32 rows of H to the down tiles of the row tile: every lane orders its
+        // stores for the async proxy and at GPU scope, then one lane counts the warp
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) red_release_gpu_add(a.ready + t.rt, 1u);
     }
 };
 
@@ -241,6 +381,30 @@ moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void*
     const int grid = row_grid(p, static_cast<int32_t>(ceil_div(p.D, kBN2)));
     return rms_sumsq ? launch_gemm<FwdDownT<true>>(ta, tb, a, grid, stream)
                      : launch_gemm<FwdDownT<false>>(ta, tb, a, grid, stream);
+}
+
+moe_status_t launch_fused_gemms(const GemmProblem& p, const int32_t* tiles2, const void* xp, const void* w13, void* h,
+                                const void* w2, const int32_t* perm, const void* scores, int32_t scores_dtype, void* y,
+                                uint32_t* ready, cudaStream_t stream) {
+    GemmMaps maps{};
+    if (!make_tmap(&maps.m[0], xp, static_cast<uint64_t>(p.D), static_cast<uint64_t>(p.R), kBK, kBM) ||
+        !make_tmap(&maps.m[1], w13, static_cast<uint64_t>(p.D), static_cast<uint64_t>(p.E) * 2 * p.F, kBK, kBN1) ||
+        !make_tmap(&maps.m[2], h, static_cast<uint64_t>(p.F), static_cast<uint64_t>(p.R), kBK, kBM) ||
+        !make_tmap(&maps.m[3], w2, static_cast<uint64_t>(p.F), static_cast<uint64_t>(p.E) * p.D, kBK, kBN2))
+        return MOE_ERR_CUDA;
+    GemmArgs a = row_args(p, p.D / kBK);
+    a.out0 = static_cast<__nv_bfloat16*>(h);  // phase 0 writes H ...
+    a.tiles_b = tiles2;
+    a.kblocks_b = p.F / kBK;
+    a.ntn = static_cast<int32_t>(ceil_div(p.F, kBN1));
+    a.ntn_b = static_cast<int32_t>(ceil_div(p.D, kBN2));
+    a.ticket = ready;       // the grid's tile counter, then (128 bytes on) one counter per row tile
+    a.ready = ready + 32;
+    a.perm = perm;
+    a.scores = scores;
+    a.scores_bf16 = scores_dtype == MOE_SCORES_BF16 ? 1 : 0;
+    a.out1 = static_cast<__nv_bfloat16*>(y);
+    return launch_gemm<FwdMega>(maps, a, row_grid(p, a.ntn + a.ntn_b), stream);
 }
 
 }  // namespace moe

@@ -42,7 +42,8 @@ moe_status_t check_shape(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, 
 
 }  // namespace
 
-bool make_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool with_activations, Layout* L) {
+bool make_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool with_activations, Layout* L,
+                 bool fused) {
     if (check_shape(T, D, F, E, K, with_activations) != MOE_OK) return false;
     const int64_t R = T * static_cast<int64_t>(K);
     L->nblk = static_cast<int>(ceil_div(R, kRouteChunk));
@@ -62,6 +63,11 @@ bool make_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool wit
         sizes[MOE_WS_XP] = 2 * static_cast<size_t>(R) * D;
         sizes[MOE_WS_H] = 2 * static_cast<size_t>(R) * F;
         sizes[MOE_WS_RMS] = sizeof(float) * static_cast<size_t>(R) * ceil_div(D, kBN2);
+        if (fused) {
+            const int64_t nonempty = R < E ? R : E;
+            sizes[MOE_WS_READY] = sizeof(uint32_t) * static_cast<size_t>(32 + ceil_div(R, kBM) + nonempty);
+            sizes[MOE_WS_Y] = 2 * static_cast<size_t>(R) * D;
+        }
     }
     size_t off = 0;
     for (int r = 0; r < MOE_WS_TOTAL; ++r) {
@@ -104,13 +110,13 @@ struct Call {
 
 // The common checks of the forward-pass stages. Host-only checks first; the device query last.
 moe_status_t prepare(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, void* workspace, size_t workspace_bytes,
-                     Call* c) {
+                     Call* c, bool fused = false) {
     moe_status_t st = check_shape(T, D, F, E, K, true);
     if (st != MOE_OK) return st;
     if (T == 0) return MOE_OK;
     if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;
-    if (!make_layout(T, D, F, E, K, true, &c->L)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!make_layout(T, D, F, E, K, true, &c->L, fused)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (workspace_bytes < c->L.off[MOE_WS_TOTAL]) return MOE_ERR_WORKSPACE_TOO_SMALL;
     c->ws = static_cast<uint8_t*>(workspace);
     c->R = T * static_cast<int64_t>(K);
@@ -401,6 +407,23 @@ moe_status_t moe_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, in
     return MOE_OK;
 }
 
+size_t moe_mega_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K) {
+    Layout L;
+    if (T == 0 || !make_layout(T, D, F, E, K, true, &L, true)) return 0;
+    return L.off[MOE_WS_TOTAL];
+}
+
+moe_status_t moe_mega_workspace_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K,
+                                       size_t* region_offsets) {
+    if (region_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, D, F, E, K, true);
+    if (st != MOE_OK) return st;
+    Layout L;
+    if (!make_layout(T, D, F, E, K, true, &L, true)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    std::memcpy(region_offsets, L.off, sizeof(L.off));
+    return MOE_OK;
+}
+
 size_t moe_routing_workspace_bytes(int64_t T, int32_t E, int32_t K) {
     Layout L;
     if (T == 0 || !make_layout(T, 0, 0, E, K, false, &L)) return 0;
@@ -582,6 +605,50 @@ moe_status_t moe_routed_experts_bwd(const void* x, const int32_t* topk_ids, cons
     p.padded_rows = L.padded_rows;
     p.sm_count = dev.sm_count;
     return launch_backward(p, s);
+}
+
+moe_status_t moe_fwd_mega_stages(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                 int32_t scores_dtype, const void* w13, const void* w2, void* out, int64_t T,
+                                 int32_t D, int32_t F, int32_t E, int32_t K, int32_t stage_begin, int32_t stage_end,
+                                 void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Call c{};
+    if (bad_scores_dtype(scores_dtype)) return MOE_ERR_INVALID_ARG;
+    if (stage_begin < 0 || stage_end > MOE_MEGA_STAGES || stage_begin > stage_end) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = prepare(T, D, F, E, K, workspace, workspace_bytes, &c, true);
+    if (st != MOE_OK || T == 0 || stage_begin == stage_end) return st;
+    const bool dispatch = stage_begin <= MOE_MEGA_STAGE_DISPATCH && MOE_MEGA_STAGE_DISPATCH < stage_end;
+    const bool gemms = stage_begin <= MOE_MEGA_STAGE_GEMMS && MOE_MEGA_STAGE_GEMMS < stage_end;
+    const bool combine = stage_begin <= MOE_MEGA_STAGE_COMBINE && MOE_MEGA_STAGE_COMBINE < stage_end;
+    if ((dispatch && !x) || !topk_ids || (gemms && (!topk_scores || !w13 || !w2)) || (combine && !out))
+        return MOE_ERR_INVALID_ARG;
+    if ((dispatch && !aligned(x, 16)) || !aligned(topk_ids, 4) ||
+        (gemms && (!aligned(w13, 16) || !aligned(w2, 16) ||
+                   !aligned(topk_scores, scores_dtype == MOE_SCORES_F32 ? 4 : 2))) ||
+        (combine && !aligned(out, 16)))
+        return MOE_ERR_MISALIGNED;
+    if ((st = check_device(&c)) != MOE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dispatch && (st = do_dispatch(c, x, topk_ids, D, F, E, K, s)) != MOE_OK) return st;
+    if (gemms) {
+        if (cudaMemsetAsync(region<uint32_t>(c, MOE_WS_READY), 0, c.L.off[MOE_WS_Y] - c.L.off[MOE_WS_READY], s) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        if ((st = launch_fused_gemms(gemm_problem(c, D, F, E, 1), region<int32_t>(c, MOE_WS_TILES2),
+                                     region<void>(c, MOE_WS_XP), w13, region<void>(c, MOE_WS_H), w2,
+                                     region<int32_t>(c, MOE_WS_PERM), topk_scores, scores_dtype,
+                                     region<void>(c, MOE_WS_Y), region<uint32_t>(c, MOE_WS_READY), s)) != MOE_OK)
+            return st;
+    }
+    if (combine) return launch_combine(region<void>(c, MOE_WS_Y), topk_ids, T, D, E, K, out, c.dev.sm_count, s);
+    return MOE_OK;
+}
+
+moe_status_t moe_routed_experts_fwd_mega(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                         int32_t scores_dtype, const void* w13, const void* w2, void* out, int64_t T,
+                                         int32_t D, int32_t F, int32_t E, int32_t K, void* workspace,
+                                         size_t workspace_bytes, moe_stream_t stream) {
+    return moe_fwd_mega_stages(x, topk_ids, topk_scores, scores_dtype, w13, w2, out, T, D, F, E, K, 0,
+                               MOE_MEGA_STAGES, workspace, workspace_bytes, stream);
 }
 
 moe_status_t moe_routed_experts_fwd_rmsnorm(const void* x, const int32_t* topk_ids, const void* topk_scores,

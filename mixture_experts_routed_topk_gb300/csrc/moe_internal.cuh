@@ -62,7 +62,9 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Host: workspace layout for the forward pass (with_activations = true) or for moe_routing alone
 // (counts/offsets/perm/inv/XP/H regions empty; those arrays are the caller's).
-bool make_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool with_activations, Layout* L);
+// fused: also the READY counters and the separate Y region of the fused forward.
+bool make_layout(int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, bool with_activations, Layout* L,
+                 bool fused = false);
 
 // Host: per-device facts, queried once per device.
 struct DeviceInfo {
@@ -110,6 +112,14 @@ moe_status_t launch_gemm1_swiglu(const GemmProblem& p, const void* xp, const voi
 moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void* w2, const int32_t* perm,
                                 const void* scores, int32_t scores_dtype, void* y, float* rms_sumsq,
                                 cudaStream_t stream);
+
+// The fused forward: both grouped GEMMs in one cooperative grid, the down tiles of a row tile
+// starting once its gate/up tiles have written their H rows. ready: the grid's tile counter, then
+// from word 32 on one uint32 per row tile (ceil(R/128) + min(R, E) of them), all zero on entry. y must not overlap xp (Y rows are written while
+// later experts' XP rows are still being read).
+moe_status_t launch_fused_gemms(const GemmProblem& p, const int32_t* tiles2, const void* xp, const void* w13, void* h,
+                                const void* w2, const int32_t* perm, const void* scores, int32_t scores_dtype, void* y,
+                                uint32_t* ready, cudaStream_t stream);
 
 // Backward pass (backward.cu): every pointer is device memory; padded_rows is the capacity of the
 // padded-row buffers (R + 127 * min(E, R), a multiple of 128).

@@ -91,6 +91,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// ------------------------------------------------------- flags between CTAs of one grid
+
+// Loads a counter with acquire semantics at GPU scope: writes released before the matching
+// increment are visible to this thread after the load observes it.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Adds to a counter with release semantics at GPU scope.
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy global accesses with the async proxy (TMA): after stores
+// that another CTA's TMA will read, and after the acquire that precedes such a TMA read.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_descriptor(const CUtensorMap* map) {

@@ -2,6 +2,7 @@
 bad arguments on the host before touching CUDA. Workspace layout arithmetic."""
 
 import ctypes
+import functools
 import os
 import re
 
@@ -48,16 +49,18 @@ def test_status_strings(lib):
 FAKE = 1 << 20  # a 256-byte-aligned non-null address; never dereferenced (host checks fail first)
 
 
-def fwd(lib, **kw):
+def fwd(lib, entry="moe_routed_experts_fwd", **kw):
     a = dict(x=FAKE, ids=FAKE, scores=FAKE, sd=0, w13=FAKE, w2=FAKE, out=FAKE,
              T=16, D=256, F=256, E=8, K=2, ws=FAKE, wsb=1 << 40)
     a.update(kw)
     v = ctypes.c_void_p
-    return lib.moe_routed_experts_fwd(v(a["x"]), v(a["ids"]), v(a["scores"]), a["sd"], v(a["w13"]), v(a["w2"]),
-                                      v(a["out"]), a["T"], a["D"], a["F"], a["E"], a["K"], v(a["ws"]), a["wsb"], None)
+    return getattr(lib, entry)(v(a["x"]), v(a["ids"]), v(a["scores"]), a["sd"], v(a["w13"]), v(a["w2"]),
+                               v(a["out"]), a["T"], a["D"], a["F"], a["E"], a["K"], v(a["ws"]), a["wsb"], None)
 
 
-def test_host_validation_needs_no_gpu(lib):
+@pytest.mark.parametrize("entry", ["moe_routed_experts_fwd", "moe_routed_experts_fwd_mega"])
+def test_host_validation_needs_no_gpu(lib, entry):
+    fwd = functools.partial(globals()["fwd"], entry=entry)
     assert fwd(lib, T=0) == OK  # nothing to do
     assert fwd(lib, T=-1) == INVALID
     assert fwd(lib, E=0) == INVALID
@@ -75,8 +78,23 @@ def test_host_validation_needs_no_gpu(lib):
     assert fwd(lib, w2=FAKE + 4) == MISALIGNED
     assert fwd(lib, ids=FAKE + 2) == MISALIGNED
     assert fwd(lib, ws=FAKE + 16) == MISALIGNED
-    need = binding.moe_workspace_bytes(16, 256, 256, 8, 2)
+    need = (binding.moe_mega_workspace_bytes if entry.endswith("mega") else binding.moe_workspace_bytes)(
+        16, 256, 256, 8, 2)
     assert fwd(lib, wsb=need - 1) == WS_SMALL
+
+
+def test_mega_stage_range_validation(lib):
+    v = ctypes.c_void_p
+    call = lambda b, e, **kw: lib.moe_fwd_mega_stages(
+        v(FAKE), v(FAKE), v(FAKE), 0, v(FAKE), v(FAKE), v(kw.get("out", FAKE)), 16, 256, 256, 8, 2, b, e,
+        v(FAKE), kw.get("wsb", 1 << 40), None)
+    assert call(-1, 2) == INVALID
+    assert call(0, 4) == INVALID
+    assert call(2, 1) == INVALID
+    assert call(1, 1) == OK  # an empty range does nothing
+    assert call(2, 3, out=0) == INVALID  # the combine stage needs out
+    assert call(2, 3, out=FAKE + 8) == MISALIGNED
+    assert call(0, 3, wsb=binding.moe_workspace_bytes(16, 256, 256, 8, 2)) == WS_SMALL  # the staged size is short
 
 
 def test_routing_host_validation(lib):
@@ -109,6 +127,26 @@ def test_workspace_layout(lib, dims):
     assert lay["status"] == 0
     assert lay["total"] == binding.moe_workspace_bytes(*dims)
     assert binding.moe_routing_workspace_bytes(T, E, K) < lay["total"]
+    # the staged layout leaves the fused forward's regions empty
+    assert lay["ready"] == lay["y"] == lay["total"]
+
+
+@pytest.mark.parametrize("dims", [(16, 256, 256, 8, 2), (4096, 2048, 1408, 64, 6), (64, 7168, 2048, 256, 8),
+                                  (1, 64, 64, 1, 1), (3, 64, 128, 4096, 7)])
+def test_mega_workspace_layout(lib, dims):
+    T, D, F, E, K = dims
+    staged = binding.moe_workspace_layout(*dims)
+    lay = binding.moe_mega_workspace_layout(*dims)
+    R = T * K
+    names = list(binding.WS_REGIONS)
+    for name in names[: names.index("ready")]:
+        assert lay[name] == staged[name], name  # the staged regions, at the same offsets
+    row_tiles = -(-R // 128) + min(R, E)
+    assert lay["y"] - lay["ready"] >= 4 * (32 + row_tiles)
+    assert lay["total"] - lay["y"] >= 2 * R * D
+    assert lay["y"] >= lay["xp"] + 2 * R * D  # Y never overlaps XP
+    assert lay["total"] == binding.moe_mega_workspace_bytes(*dims)
+    assert binding.moe_mega_workspace_bytes(0, D, F, E, K) == 0
 
 
 def bwd(lib, **kw):

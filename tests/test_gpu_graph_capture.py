@@ -19,7 +19,7 @@ def problem(T, D, F, E, K, seed):
     return to_device(d)
 
 
-@pytest.mark.parametrize("precision", ["bf16", "mxfp8", "nvfp4"])
+@pytest.mark.parametrize("precision", ["bf16", "mega", "mxfp8", "nvfp4"])
 def test_forward_replays_from_a_cuda_graph(precision):
     T, D, F, E, K = 200, 256, 384, 6, 3
     d = problem(T, D, F, E, K, seed=11)
@@ -30,6 +30,9 @@ def test_forward_replays_from_a_cuda_graph(precision):
     if precision == "bf16":
         ws = binding.alloc_workspace(binding.moe_workspace_bytes(T, D, F, E, K))
         call = lambda s: binding.moe_routed_experts_fwd(x, ids, sc, d["w13"], d["w2"], out, ws, stream=s)
+    elif precision == "mega":  # the fused forward: a cooperative launch inside the graph
+        ws = binding.alloc_workspace(binding.moe_mega_workspace_bytes(T, D, F, E, K))
+        call = lambda s: binding.moe_routed_experts_fwd_mega(x, ids, sc, d["w13"], d["w2"], out, ws, stream=s)
     elif precision == "mxfp8":
         w13 = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W13, d["w13"])
         w2 = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W2, d["w2"])

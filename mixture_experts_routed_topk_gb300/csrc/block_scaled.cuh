@@ -36,7 +36,14 @@ __device__ __forceinline__ MxTile decode_mx_tile(int32_t tile, const GemmArgs& a
     return t;
 }
 
-// Blocks of 8 warps (one row each) for the quantization kernels, at most 8 per SM.
+// Columns per work item of the token-order gathers: whole rows (rounded up to 1024) when the batch
+// alone fills the GPU, else 1024-column chunks, so a small batch still spreads over every SM
+// (a chunk recomputes its token's destination rows, which costs about 10 % on large batches).
+int32_t gather_chunk_cols(int64_t T, int32_t cols) {
+    return T >= 2048 ? (cols + 1023) / 1024 * 1024 : 1024;
+}
+
+// Blocks of 8 warps (one work item each) for the quantization kernels, at most 8 per SM.
 int quant_grid(int64_t rows, int sm_count) {
     const int64_t want = (rows + 7) / 8;  // 8 warps per block, one row each
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;

@@ -151,7 +151,7 @@ constexpr int kEpilogueStagingBytes = (kEpilogueThreads / 32) * 32 * kStageRowU4
 constexpr int kTileRing = 4;  // tiles in flight between producer and consumers (dynamic schedule)
 constexpr int kTileStoreBytes = 32;
 
-struct alignas(8) PipeState {
+struct alignas(16) PipeState {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t acc_full[2];

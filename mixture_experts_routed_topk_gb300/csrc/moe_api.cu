@@ -170,7 +170,7 @@ moe_status_t do_dispatch(const Call& c, const void* x, const int32_t* ids, int32
     b.status = region<uint32_t>(c, MOE_WS_STATUS);
     moe_status_t st = launch_routing(b, stream);
     if (st != MOE_OK) return st;
-    return launch_gather(x, b.perm, b.offsets, E, K, c.R, D, region<void>(c, MOE_WS_XP), c.dev.sm_count, stream);
+    return launch_gather(x, b.inv, b.offsets, E, K, c.R, D, region<void>(c, MOE_WS_XP), c.dev.sm_count, stream);
 }
 
 moe_status_t do_gemm1(const Call& c, const void* w13, int32_t D, int32_t F, int32_t E, cudaStream_t stream) {

@@ -93,7 +93,8 @@ struct RoutingBuffers {
 };
 moe_status_t launch_routing(const RoutingBuffers& b, cudaStream_t stream);
 
-moe_status_t launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int32_t E, int32_t K,
+// XP[inv[t*K+k]] = x[t] for the valid pairs (token order: each x row is read once).
+moe_status_t launch_gather(const void* x, const int32_t* inv, const int32_t* offsets, int32_t E, int32_t K,
                            int64_t R, int32_t D, void* xp, int sm_count, cudaStream_t stream);
 
 struct GemmProblem {

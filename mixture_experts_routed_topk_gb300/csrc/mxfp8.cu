@@ -9,7 +9,7 @@
 //
 // Kernels, in stream order (weights prepared beforehand by k_mx_prepare_weight):
 //   routing (shared with the bf16 path; row-tile prefix tiles[e] = sum ceil(n_e' / 128))
-//   -> k_mx_gather_quant: x rows in routed order -> XQ codes + scales, every expert's rows
+//   -> k_mx_gather_quant: x rows, quantized once per token -> XQ codes + scales, every expert's rows
 //      starting on a 128-row boundary ("padded rows"), so a row tile's scales are one chunk
 //   -> gate/up GEMM (block-scaled tcgen05): H = SiLU(g) * u from the fp32 accumulators,
 //      quantized per 32 f in the epilogue -> HQ codes + scales
@@ -51,11 +51,44 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, f
     return (lo & 0xffffu) | (hi << 16);
 }
 
+// One 256-column step of a warp's row quantization: lane l takes the 8 values at c = c0 + 8 l
+// (zeros past cols), lanes 4j .. 4j+3 share one 32-value block. Returns the lane's 8 E4M3 codes;
+// word = the four UE8M0 codes of the 128-column group starting at c0 + 8 (l & 16), valid in lanes
+// with (l & 15) == 0.
+__device__ __forceinline__ uint2 mx_quantize_step(const uint4* src, int cols, int c0, uint32_t& word) {
+    const int lane = threadIdx.x & 31;
+    const int c = c0 + lane * 8;
+    float v[8];
+    if (c < cols) {
+        const uint4 q = __ldg(src + c / 8);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int e = mx_exponent(amax);
+    const float m = mx_inv_scale(e);
+    const uint32_t code = static_cast<uint32_t>(e + 127);
+    const int base = lane & 16;
+    word = __shfl_sync(0xffffffffu, code, base) | (__shfl_sync(0xffffffffu, code, base + 4) << 8) |
+           (__shfl_sync(0xffffffffu, code, base + 8) << 16) | (__shfl_sync(0xffffffffu, code, base + 12) << 24);
+    return make_uint2(e4m3x4(v[0], v[1], v[2], v[3], m), e4m3x4(v[4], v[5], v[6], v[7], m));
+}
+
 // One warp quantizes one row of `cols` bf16 values (cols % 128 == 0; src null = a zero row: zero
 // codes and the all-zero block's scale code 0, written directly) into
 // E4M3 codes at dst and UE8M0 scales: the four scales of 128-column group g go, as one 32-bit
-// word, to sf_row + g * sf_group_stride. Lane l handles 8 consecutive values per 256-column step;
-// lanes 4j .. 4j+3 share one 32-value block.
+// word, to sf_row + g * sf_group_stride.
 __device__ __forceinline__ void warp_quantize_row(const uint4* src, uint8_t* dst, int cols, uint8_t* sf_row,
                                                   int64_t sf_group_stride) {
     const int lane = threadIdx.x & 31;
@@ -66,38 +99,34 @@ __device__ __forceinline__ void warp_quantize_row(const uint4* src, uint8_t* dst
         return;
     }
     for (int c0 = 0; c0 < cols; c0 += 256) {
+        uint32_t word;
+        const uint2 codes = mx_quantize_step(src, cols, c0, word);
         const int c = c0 + lane * 8;
-        const bool active = c < cols;
-        float v[8];
-        if (active) {
-            const uint4 q = __ldg(src + c / 8);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[2 * i] = __uint_as_float(w[i] << 16);
-                v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        if (c < cols) *reinterpret_cast<uint2*>(dst + c) = codes;
+        if ((lane & 15) == 0 && c < cols) *reinterpret_cast<uint32_t*>(sf_row + static_cast<int64_t>(c / 128) * sf_group_stride) = word;
+    }
+}
+
+// Columns [c_begin, c_end) of a token's row (c_begin a multiple of 256), quantized once and written
+// to up to 32 padded rows of XQ / XS: lane k < nk holds the k-th destination row (-1: none).
+// Scales of padded row r, group g: chunk (r / 128, g) of a [rows / 128, groups] grid of 512-byte
+// chunks, byte sf_in_chunk(r, 0) of it.
+__device__ __forceinline__ void warp_quantize_row_to_rows(const uint4* src, int cols, int c_begin, int c_end,
+                                                          int64_t dst_row, int nk, uint8_t* xq, uint8_t* xs) {
+    const int lane = threadIdx.x & 31;
+    const int groups = cols / 128;
+    for (int c0 = c_begin; c0 < c_end && c0 < cols; c0 += 256) {
+        uint32_t word;
+        const uint2 codes = mx_quantize_step(src, cols, c0, word);
+        const int c = c0 + lane * 8;
+        for (int k = 0; k < nk; ++k) {
+            const int64_t prow = __shfl_sync(0xffffffffu, dst_row, k);
+            if (prow < 0) continue;  // warp-uniform
+            if (c < cols) *reinterpret_cast<uint2*>(xq + prow * cols + c) = codes;
+            if ((lane & 15) == 0 && c < cols)
+                *reinterpret_cast<uint32_t*>(xs + ((prow >> 7) * groups + c / 128) * 512 +
+                                             sf_in_chunk(static_cast<int>(prow & 127), 0)) = word;
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const int e = mx_exponent(amax);
-        const float m = mx_inv_scale(e);
-        if (active)
-            *reinterpret_cast<uint2*>(dst + c) =
-                make_uint2(e4m3x4(v[0], v[1], v[2], v[3], m), e4m3x4(v[4], v[5], v[6], v[7], m));
-        const uint32_t code = static_cast<uint32_t>(e + 127);
-        const int base = lane & 16;
-        const uint32_t word = __shfl_sync(0xffffffffu, code, base) | (__shfl_sync(0xffffffffu, code, base + 4) << 8) |
-                              (__shfl_sync(0xffffffffu, code, base + 8) << 16) |
-                              (__shfl_sync(0xffffffffu, code, base + 12) << 24);
-        if ((lane & 15) == 0 && active)
-            *reinterpret_cast<uint32_t*>(sf_row + static_cast<int64_t>((c0 + base * 8) / 128) * sf_group_stride) = word;
     }
 }
 
@@ -135,41 +164,57 @@ __global__ void __launch_bounds__(256) k_mx_prepare_weight(const uint4* __restri
     }
 }
 
-// XQ[prow] = MX(x[t]) for every padded row: prow = 128 tiles[e] + i holds routed row
-// r = offsets[e] + i of expert e (pair p = perm[r], token t = p / K) when i < counts[e], and zeros
-// (codes 0, scale 2^-127) for the padding after the expert's rows. One warp per padded row.
-__global__ void __launch_bounds__(256) k_mx_gather_quant(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
+// XQ in token order. Work item i < T * chunks: chunk i % chunks (chunk_cols columns, a multiple of
+// 1024: whole rows for large batches, 1024 columns for small ones) of x[t], t = i / chunks,
+// is quantized once and written to the padded row of each of the token's valid pairs (pair
+// p = t K + k of expert e = ids[p] sits at padded row 128 tiles[e] + inv[p] - offsets[e]), so x is
+// read once per token, not once per pair. The next 128 E items fill padded row
+// 128 tiles[e] + counts[e] + j when it lies in expert e's last row tile: zero codes and scale
+// 2^-127. One warp per item.
+__global__ void __launch_bounds__(256) k_mx_gather_quant(const uint4* __restrict__ x, const int32_t* __restrict__ ids,
+                                                         const int32_t* __restrict__ inv,
                                                          const int32_t* __restrict__ counts,
                                                          const int32_t* __restrict__ offsets,
                                                          const int32_t* __restrict__ tiles, int32_t E, int32_t K,
-                                                         int32_t D, uint8_t* __restrict__ xq,
-                                                         uint8_t* __restrict__ xs) {
-    extern __shared__ int32_t s_tiles[];  // tiles[0 .. E], so each row's expert lookup stays on chip
+                                                         int64_t T, int32_t D, int32_t chunk_cols,
+                                                         uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+    extern __shared__ int32_t s_tiles[];  // tiles[0 .. E], the padded-row base of every expert
     griddep_wait();
     griddep_launch_dependents();
     for (int i = threadIdx.x; i <= E; i += blockDim.x) s_tiles[i] = __ldg(tiles + i);
     __syncthreads();
-    const int64_t rows = 128 * static_cast<int64_t>(s_tiles[E]);
+    const int lane = threadIdx.x & 31;
+    const int chunks = (D + chunk_cols - 1) / chunk_cols;
+    const int64_t token_items = T * chunks;
+    const int64_t items = token_items + 128 * static_cast<int64_t>(E);
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const int groups = D / 128;
-    for (int64_t prow = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); prow < rows;
-         prow += warps_total) {
-        const int32_t tile = static_cast<int32_t>(prow >> 7);
-        int lo = 0, hi = E - 1;  // the last expert e with tiles[e] <= tile (empty experts are skipped)
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_tiles[mid] <= tile) lo = mid;
-            else hi = mid - 1;
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
+         item += warps_total) {
+        if (item < token_items) {
+            const int64_t t = item / chunks;
+            const int c_begin = static_cast<int>(item - t * chunks) * chunk_cols;
+            for (int k0 = 0; k0 < K; k0 += 32) {
+                const int nk = min(32, K - k0);
+                int64_t dst_row = -1;
+                if (lane < nk) {
+                    const int64_t p = t * K + k0 + lane;
+                    const int32_t e = __ldg(ids + p);
+                    if (e >= 0 && e < E)
+                        dst_row = 128 * static_cast<int64_t>(s_tiles[e]) + __ldg(inv + p) - __ldg(offsets + e);
+                }
+                warp_quantize_row_to_rows(x + t * (D / 8), D, c_begin, c_begin + chunk_cols, dst_row, nk, xq, xs);
+            }
+        } else {
+            const int32_t e = static_cast<int32_t>((item - token_items) >> 7);
+            const int32_t j = static_cast<int32_t>((item - token_items) & 127);
+            const int32_t n = __ldg(counts + e);
+            if (n + j < 128 * (s_tiles[e + 1] - s_tiles[e])) {
+                const int64_t prow = 128 * static_cast<int64_t>(s_tiles[e]) + n + j;
+                warp_quantize_row(nullptr, xq + prow * D, D,
+                                  xs + (prow >> 7) * (D / 128) * 512 + sf_in_chunk(static_cast<int>(prow & 127), 0),
+                                  512);
+            }
         }
-        const int32_t e = lo;
-        const int64_t i = prow - 128 * static_cast<int64_t>(s_tiles[e]);
-        const uint4* src = nullptr;
-        if (i < __ldg(counts + e)) {
-            const int32_t p = __ldg(perm + __ldg(offsets + e) + i);
-            src = x + static_cast<int64_t>(p / K) * (D / 8);
-        }
-        uint8_t* sf_row = xs + (prow >> 7) * groups * 512 + sf_in_chunk(static_cast<int>(prow & 127), 0);
-        warp_quantize_row(src, xq + prow * D, D, sf_row, 512);
     }
 }
 
@@ -318,11 +363,13 @@ moe_status_t mx_dispatch(const MxProblem& p, cudaStream_t stream) {
     b.status = p.status;
     moe_status_t st = launch_routing(b, stream);
     if (st != MOE_OK) return st;
-    return launch_pdl(k_mx_gather_quant, dim3(quant_grid(p.padded_rows, p.sm_count)), dim3(256),
-                      sizeof(int32_t) * (p.E + 1), stream,
-                      static_cast<const uint4*>(p.x), static_cast<const int32_t*>(p.perm),
-                      static_cast<const int32_t*>(p.counts), static_cast<const int32_t*>(p.offsets),
-                      static_cast<const int32_t*>(p.tiles1), p.E, p.K, p.D, p.xq, p.xs) == cudaSuccess
+    const int32_t chunk = gather_chunk_cols(p.T, p.D);
+    return launch_pdl(k_mx_gather_quant,
+                      dim3(quant_grid(p.T * ((p.D + chunk - 1) / chunk) + 128 * static_cast<int64_t>(p.E), p.sm_count)),
+                      dim3(256), sizeof(int32_t) * (p.E + 1), stream, static_cast<const uint4*>(p.x), p.ids,
+                      static_cast<const int32_t*>(p.inv), static_cast<const int32_t*>(p.counts),
+                      static_cast<const int32_t*>(p.offsets), static_cast<const int32_t*>(p.tiles1), p.E, p.K, p.T,
+                      p.D, chunk, p.xq, p.xs) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
 }

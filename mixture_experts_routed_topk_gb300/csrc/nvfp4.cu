@@ -10,7 +10,8 @@
 // SwiGLU output h) are calibration constants given by the caller.
 //
 // Kernels, in stream order (weights prepared beforehand: k_nv_amax, k_nv_prepare_weight):
-//   routing -> k_nv_gather_quant (x rows at padded rows, packed E2M1 + UE4M3 chunks)
+//   routing -> k_nv_gather_quant (x rows, quantized once per token, at padded rows: packed E2M1 +
+//   UE4M3 chunks)
 //   -> gate/up GEMM (kind::mxf4nvf4, 128 x 128 tiles of 64 gate + 64 up columns): g and u scaled
 //      by G_x G_w13 in fp32, h = SiLU(g) u quantized per 16 f with G_h -> HQ, HS
 //   -> down GEMM (128 x 128 tiles of D): Y[perm[r]] = score G_h G_w2 acc, bf16
@@ -67,6 +68,33 @@ __device__ __forceinline__ uint32_t nv_block(const float (&v)[16], float G, floa
     return s;
 }
 
+// One 512-column step of a warp's row quantization: lane l takes the 16 values at c = c0 + 16 l
+// (zeros past cols) as one block and returns its packed codes; word = the four UE4M3 codes of
+// lanes 4j .. 4j+3 (valid in lanes with (l & 3) == 0).
+__device__ __forceinline__ uint2 nv_quantize_step(const uint4* src, int cols, int c0, float G, float t6g, uint32_t& word) {
+    const int lane = threadIdx.x & 31;
+    const int c = c0 + lane * 16;
+    float v[16];
+    if (c < cols) {
+        const uint4 q0 = __ldg(src + c / 8), q1 = __ldg(src + c / 8 + 1);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+    }
+    uint2 packed;
+    const uint32_t s = nv_block(v, G, t6g, packed);
+    const int base = lane & ~3;
+    word = __shfl_sync(0xffffffffu, s, base) | (__shfl_sync(0xffffffffu, s, base + 1) << 8) |
+           (__shfl_sync(0xffffffffu, s, base + 2) << 16) | (__shfl_sync(0xffffffffu, s, base + 3) << 24);
+    return packed;
+}
+
 // One warp quantizes one row of `cols` bf16 values (cols % 128 == 0) into packed E2M1 codes at dst
 // (cols / 2 bytes) and UE4M3 scales: the four scales of 64-column group g go, as one 32-bit word,
 // to sf_row + g * sf_group_stride, for g < nv_groups(cols) (zero words for the padding groups).
@@ -83,30 +111,37 @@ __device__ __forceinline__ void warp_quantize_row_nv(const uint4* src, uint8_t* 
     }
     const int cols_pad = nv_groups(cols) * 64;
     for (int c0 = 0; c0 < cols_pad; c0 += 512) {
+        uint32_t word;
+        const uint2 packed = nv_quantize_step(src, cols, c0, G, t6g, word);
         const int c = c0 + lane * 16;
-        const bool data = c < cols;
-        float v[16];
-        if (data) {
-            const uint4 q0 = __ldg(src + c / 8), q1 = __ldg(src + c / 8 + 1);
-            const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                v[2 * i] = __uint_as_float(w[i] << 16);
-                v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-        }
-        uint2 packed;
-        const uint32_t s = nv_block(v, G, t6g, packed);
-        if (data) *reinterpret_cast<uint2*>(dst + c / 2) = packed;
-        const int base = lane & ~3;
-        const uint32_t word = __shfl_sync(0xffffffffu, s, base) | (__shfl_sync(0xffffffffu, s, base + 1) << 8) |
-                              (__shfl_sync(0xffffffffu, s, base + 2) << 16) |
-                              (__shfl_sync(0xffffffffu, s, base + 3) << 24);
+        if (c < cols) *reinterpret_cast<uint2*>(dst + c / 2) = packed;
         if ((lane & 3) == 0 && c < cols_pad)
             *reinterpret_cast<uint32_t*>(sf_row + static_cast<int64_t>(c / 64) * sf_group_stride) = word;
+    }
+}
+
+// Columns [c_begin, c_end) of a token's row, padded to whole 256-wide groups (c_begin a multiple of
+// 512), quantized once and written to up to 32 padded rows of XQ / XS: lane k < nk holds the k-th
+// destination row (-1: none). Scales of padded row r, group g: chunk (r / 128, g) of a
+// [rows / 128, nv_groups(cols)] grid of 512-byte chunks, byte sf_in_chunk(r, 0) of it.
+__device__ __forceinline__ void warp_quantize_row_nv_to_rows(const uint4* src, int cols, int c_begin, int c_end,
+                                                             float G, float t6g, int64_t dst_row, int nk, uint8_t* xq,
+                                                             uint8_t* xs) {
+    const int lane = threadIdx.x & 31;
+    const int groups = nv_groups(cols);
+    const int cols_pad = groups * 64;
+    for (int c0 = c_begin; c0 < c_end && c0 < cols_pad; c0 += 512) {
+        uint32_t word;
+        const uint2 packed = nv_quantize_step(src, cols, c0, G, t6g, word);
+        const int c = c0 + lane * 16;
+        for (int k = 0; k < nk; ++k) {
+            const int64_t prow = __shfl_sync(0xffffffffu, dst_row, k);
+            if (prow < 0) continue;  // warp-uniform
+            if (c < cols) *reinterpret_cast<uint2*>(xq + prow * (cols / 2) + c / 2) = packed;
+            if ((lane & 3) == 0 && c < cols_pad)
+                *reinterpret_cast<uint32_t*>(xs + ((prow >> 7) * groups + c / 64) * 512 +
+                                             sf_in_chunk(static_cast<int>(prow & 127), 0)) = word;
+        }
     }
 }
 
@@ -181,42 +216,58 @@ __global__ void __launch_bounds__(256) k_nv_prepare_weight(const uint4* __restri
     }
 }
 
-// XQ[prow] = NVFP4(x[t], G_x) for every padded row (routed row offsets[e] + i of expert e at
-// prow = 128 tiles[e] + i when i < counts[e]); padding rows get zero scales (their codes are not
-// written). One warp per padded row.
-__global__ void __launch_bounds__(256) k_nv_gather_quant(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
+// XQ in token order, as the MXFP8 gather: item i < T * chunks quantizes chunk i % chunks
+// (chunk_cols columns of the row padded to whole 256-wide groups) of x[i / chunks] once (tensor scale gx)
+// and writes it to the padded row of each of the token's valid pairs; the next 128 E items clear
+// the scale words of padded row 128 tiles[e] + counts[e] + j when it lies in expert e's last row
+// tile (a zero scale makes every product 0, whatever the codes). One warp per item.
+__global__ void __launch_bounds__(256) k_nv_gather_quant(const uint4* __restrict__ x, const int32_t* __restrict__ ids,
+                                                         const int32_t* __restrict__ inv,
                                                          const int32_t* __restrict__ counts,
                                                          const int32_t* __restrict__ offsets,
                                                          const int32_t* __restrict__ tiles, int32_t E, int32_t K,
-                                                         int32_t D, float gx, uint8_t* __restrict__ xq,
-                                                         uint8_t* __restrict__ xs) {
-    extern __shared__ int32_t s_tiles[];  // tiles[0 .. E], so each row's expert lookup stays on chip
+                                                         int64_t T, int32_t D, int32_t chunk_cols, float gx,
+                                                         uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+    extern __shared__ int32_t s_tiles[];  // tiles[0 .. E], the padded-row base of every expert
     griddep_wait();
     griddep_launch_dependents();
     for (int i = threadIdx.x; i <= E; i += blockDim.x) s_tiles[i] = __ldg(tiles + i);
     __syncthreads();
-    const int64_t rows = 128 * static_cast<int64_t>(s_tiles[E]);
-    const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int lane = threadIdx.x & 31;
     const int groups = nv_groups(D);
     const float t6g = __fmul_rn(6.0f, gx);
-    for (int64_t prow = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); prow < rows;
-         prow += warps_total) {
-        const int32_t tile = static_cast<int32_t>(prow >> 7);
-        int lo = 0, hi = E - 1;  // the last expert e with tiles[e] <= tile (empty experts are skipped)
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_tiles[mid] <= tile) lo = mid;
-            else hi = mid - 1;
+    const int chunks = (groups * 64 + chunk_cols - 1) / chunk_cols;
+    const int64_t token_items = T * chunks;
+    const int64_t items = token_items + 128 * static_cast<int64_t>(E);
+    const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
+         item += warps_total) {
+        if (item < token_items) {
+            const int64_t t = item / chunks;
+            const int c_begin = static_cast<int>(item - t * chunks) * chunk_cols;
+            for (int k0 = 0; k0 < K; k0 += 32) {
+                const int nk = min(32, K - k0);
+                int64_t dst_row = -1;
+                if (lane < nk) {
+                    const int64_t p = t * K + k0 + lane;
+                    const int32_t e = __ldg(ids + p);
+                    if (e >= 0 && e < E)
+                        dst_row = 128 * static_cast<int64_t>(s_tiles[e]) + __ldg(inv + p) - __ldg(offsets + e);
+                }
+                warp_quantize_row_nv_to_rows(x + t * (D / 8), D, c_begin, c_begin + chunk_cols, gx, t6g, dst_row, nk,
+                                             xq, xs);
+            }
+        } else {
+            const int32_t e = static_cast<int32_t>((item - token_items) >> 7);
+            const int32_t j = static_cast<int32_t>((item - token_items) & 127);
+            const int32_t n = __ldg(counts + e);
+            if (n + j < 128 * (s_tiles[e + 1] - s_tiles[e])) {
+                const int64_t prow = 128 * static_cast<int64_t>(s_tiles[e]) + n + j;
+                warp_quantize_row_nv(nullptr, xq + prow * (D / 2), D, gx, t6g,
+                                     xs + (prow >> 7) * groups * 512 + sf_in_chunk(static_cast<int>(prow & 127), 0),
+                                     512);
+            }
         }
-        const int32_t e = lo;
-        const int64_t i = prow - 128 * static_cast<int64_t>(s_tiles[e]);
-        const uint4* src = nullptr;
-        if (i < __ldg(counts + e)) {
-            const int32_t p = __ldg(perm + __ldg(offsets + e) + i);
-            src = x + static_cast<int64_t>(p / K) * (D / 8);
-        }
-        uint8_t* sf_row = xs + (prow >> 7) * groups * 512 + sf_in_chunk(static_cast<int>(prow & 127), 0);
-        warp_quantize_row_nv(src, xq + prow * (D / 2), D, gx, t6g, sf_row, 512);
     }
 }
 
@@ -356,11 +407,14 @@ moe_status_t nv_dispatch(const MxProblem& p, cudaStream_t stream) {
     b.status = p.status;
     moe_status_t st = launch_routing(b, stream);
     if (st != MOE_OK) return st;
-    return launch_pdl(k_nv_gather_quant, dim3(quant_grid(p.padded_rows, p.sm_count)), dim3(256),
-                      sizeof(int32_t) * (p.E + 1), stream,
-                      static_cast<const uint4*>(p.x), static_cast<const int32_t*>(p.perm),
-                      static_cast<const int32_t*>(p.counts), static_cast<const int32_t*>(p.offsets),
-                      static_cast<const int32_t*>(p.tiles1), p.E, p.K, p.D, p.act_scale_x, p.xq, p.xs) == cudaSuccess
+    const int32_t chunk = gather_chunk_cols(p.T, nv_groups(p.D) * 64);
+    return launch_pdl(k_nv_gather_quant,
+                      dim3(quant_grid(p.T * ((nv_groups(p.D) * 64 + chunk - 1) / chunk) + 128 * static_cast<int64_t>(p.E),
+                                      p.sm_count)),
+                      dim3(256), sizeof(int32_t) * (p.E + 1), stream, static_cast<const uint4*>(p.x), p.ids,
+                      static_cast<const int32_t*>(p.inv), static_cast<const int32_t*>(p.counts),
+                      static_cast<const int32_t*>(p.offsets), static_cast<const int32_t*>(p.tiles1), p.E, p.K, p.T,
+                      p.D, chunk, p.act_scale_x, p.xq, p.xs) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
 }

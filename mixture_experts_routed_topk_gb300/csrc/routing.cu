@@ -179,26 +179,37 @@ __global__ void __launch_bounds__(kRouteWarps * 32) k_route_permute(const int32_
     }
 }
 
-// Gather: XP[r, :] = x[perm[r] / K, :] for the valid rows r < offsets[E]; one warp per row,
-// 16-byte vectors, four loads in flight per lane.
-__global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
+// Gather: XP[inv[t*K+k], :] = x[t, :] for every pair whose row is valid (< offsets[E]). A work item
+// is one 1024-column chunk of one token (one warp, 16-byte vectors, four per lane): it reads the
+// chunk of x[t] once and writes it to each of the token's K rows, so x is read once instead of
+// once per pair (K times the bytes when x does not fit in L2), and a small batch still has
+// tokens x chunks items to spread over the GPU.
+constexpr int kGatherChunkVec = 128;  // 16-byte vectors per chunk (1024 bf16)
+
+__global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ inv,
                                                      const int32_t* __restrict__ offsets, int32_t E, int32_t K,
-                                                     int vec_per_row, uint4* __restrict__ xp) {
+                                                     int64_t T, int vec_per_row, uint4* __restrict__ xp) {
     griddep_wait();
     griddep_launch_dependents();
-    const int64_t nvalid = __ldg(offsets + E);
+    const int32_t nvalid = __ldg(offsets + E);
     const int lane = threadIdx.x & 31;
+    const int chunks = (vec_per_row + kGatherChunkVec - 1) / kGatherChunkVec;
+    const int64_t items = T * chunks;
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nvalid;
-         r += warps_total) {
-        const int64_t t = __ldg(perm + r) / K;
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
+         item += warps_total) {
+        const int64_t t = item / chunks;
+        const int j = static_cast<int>(item - t * chunks) * kGatherChunkVec + lane;
         const uint4* src = x + t * vec_per_row;
-        uint4* dst = xp + r * vec_per_row;
-        for (int j = lane; j < vec_per_row; j += 128) {
-            uint4 v[4];
+        uint4 v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (j + u * 32 < vec_per_row) v[u] = __ldg(src + j + u * 32);
+        for (int u = 0; u < 4; ++u)
+            if (j + u * 32 < vec_per_row) v[u] = __ldg(src + j + u * 32);
+        const int32_t* rows = inv + t * K;
+        for (int k = 0; k < K; ++k) {
+            const int32_t row = __ldg(rows + k);
+            if (row >= nvalid) continue;  // a pair with an invalid id (warp-uniform)
+            uint4* dst = xp + static_cast<int64_t>(row) * vec_per_row;
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (j + u * 32 < vec_per_row) dst[j + u * 32] = v[u];
@@ -233,13 +244,14 @@ moe_status_t launch_routing(const RoutingBuffers& b, cudaStream_t stream) {
     return MOE_OK;
 }
 
-moe_status_t launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int32_t E, int32_t K,
+moe_status_t launch_gather(const void* x, const int32_t* inv, const int32_t* offsets, int32_t E, int32_t K,
                            int64_t R, int32_t D, void* xp, int sm_count, cudaStream_t stream) {
     const int vec_per_row = D / 8;
-    const int64_t want = ceil_div(R, 8);  // one warp per row, 8 warps per block
+    const int64_t T = R / K;
+    const int64_t want = ceil_div(T * ceil_div(vec_per_row, kGatherChunkVec), 8);  // one warp per item, 8 per block
     const int grid = static_cast<int>(want < static_cast<int64_t>(sm_count) * 8 ? want : static_cast<int64_t>(sm_count) * 8);
-    return launch_pdl(k_gather_rows, dim3(grid > 0 ? grid : 1), dim3(256), 0, stream, static_cast<const uint4*>(x), perm,
-                      offsets, E, K, vec_per_row, static_cast<uint4*>(xp)) == cudaSuccess
+    return launch_pdl(k_gather_rows, dim3(grid > 0 ? grid : 1), dim3(256), 0, stream, static_cast<const uint4*>(x), inv,
+                      offsets, E, K, T, vec_per_row, static_cast<uint4*>(xp)) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
 }

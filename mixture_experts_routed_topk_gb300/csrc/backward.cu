@@ -15,7 +15,7 @@
 // GEMMs, which contract over an expert's rows, never read another expert's rows.
 //
 // Kernels, in stream order:
-//   routing (shared with the forward) -> k_pad_tiles -> k_pad_rows -> k_gather_bwd
+//   routing (shared with the forward) -> k_pad_tiles -> k_pad_rows -> k_gather_bwd (token order)
 //   -> recompute (A = XPP rows, B = w13): GU = [g | u], HS = s h
 //   -> dgrad of the down projection (A = DOP rows, B = W2 read MN-major): q = dout W2, with the
 //      SwiGLU backward in the epilogue: DGU = [dg | du] and partial dscores per column tile
@@ -90,46 +90,56 @@ __global__ void __launch_bounds__(256) k_pad_rows(const int32_t* __restrict__ id
     }
 }
 
-// XPP[prow] = x[t], DOP[prow] = dout[t] for the pair of padded row prow (t = pair / K); zeros for
-// padding rows. One warp per row, 16-byte vectors.
+// XPP[pinv[p]] = x[t], DOP[pinv[p]] = dout[t] for every valid pair p = t K + k, in token order: a
+// work item is one 1024-column chunk of one token (one warp, 16-byte vectors, four per lane per
+// tensor), read once and written to each of the token's K padded rows, so x and dout are read
+// once instead of once per pair. The next 128 * pmt[E] items zero the padding rows (pperm < 0).
+constexpr int kGatherChunkVec = 128;  // 16-byte vectors per chunk
+
 __global__ void __launch_bounds__(256) k_gather_bwd(const uint4* __restrict__ x, const uint4* __restrict__ dout,
                                                     const int32_t* __restrict__ pperm,
-                                                    const int32_t* __restrict__ pmt, int32_t E, int32_t K,
+                                                    const int32_t* __restrict__ pinv,
+                                                    const int32_t* __restrict__ pmt, int32_t E, int32_t K, int64_t T,
                                                     int vec_per_row, uint4* __restrict__ xpp,
                                                     uint4* __restrict__ dop) {
     griddep_wait();
     griddep_launch_dependents();
     const int64_t rows = static_cast<int64_t>(kPadRows) * __ldg(pmt + E);
     const int lane = threadIdx.x & 31;
+    const int chunks = (vec_per_row + kGatherChunkVec - 1) / kGatherChunkVec;
+    const int64_t token_items = T * chunks;
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-         r += warps_total) {
-        const int32_t p = __ldg(pperm + r);
-        uint4* dx = xpp + r * vec_per_row;
-        uint4* dd = dop + r * vec_per_row;
-        if (p < 0) {
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         item < token_items + rows; item += warps_total) {
+        if (item < token_items) {
+            const int64_t t = item / chunks;
+            const int j = static_cast<int>(item - t * chunks) * kGatherChunkVec + lane;
+            uint4 a[4], b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j + u * 32 < vec_per_row) {
+                    a[u] = __ldg(x + t * vec_per_row + j + u * 32);
+                    b[u] = __ldg(dout + t * vec_per_row + j + u * 32);
+                }
+            for (int k = 0; k < K; ++k) {
+                const int32_t prow = __ldg(pinv + t * K + k);
+                if (prow < 0) continue;  // a pair with an invalid id (warp-uniform)
+                uint4* dx = xpp + static_cast<int64_t>(prow) * vec_per_row;
+                uint4* dd = dop + static_cast<int64_t>(prow) * vec_per_row;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (j + u * 32 < vec_per_row) {
+                        dx[j + u * 32] = a[u];
+                        dd[j + u * 32] = b[u];
+                    }
+            }
+        } else {
+            const int64_t r = item - token_items;
+            if (__ldg(pperm + r) >= 0) continue;
             const uint4 z = make_uint4(0, 0, 0, 0);
             for (int j = lane; j < vec_per_row; j += 32) {
-                dx[j] = z;
-                dd[j] = z;
-            }
-            continue;
-        }
-        const int64_t t = p / K;
-        const uint4* sx = x + t * vec_per_row;
-        const uint4* sd = dout + t * vec_per_row;
-        for (int j = lane; j < vec_per_row; j += 64) {
-            uint4 a0 = __ldg(sx + j), b0 = __ldg(sd + j), a1, b1;
-            const bool two = j + 32 < vec_per_row;
-            if (two) {
-                a1 = __ldg(sx + j + 32);
-                b1 = __ldg(sd + j + 32);
-            }
-            dx[j] = a0;
-            dd[j] = b0;
-            if (two) {
-                dx[j + 32] = a1;
-                dd[j + 32] = b1;
+                xpp[r * vec_per_row + j] = z;
+                dop[r * vec_per_row + j] = z;
             }
         }
     }
@@ -487,10 +497,11 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
         launch_pdl(k_pad_rows, dim3(grid_for(R, 256, p.sm_count)), dim3(256), 0, stream, p.ids,
                    static_cast<const int32_t*>(p.inv), static_cast<const int32_t*>(p.offsets),
                    static_cast<const int32_t*>(p.pmt), R, E, p.pperm, p.pinv) != cudaSuccess ||
-        launch_pdl(k_gather_bwd, dim3(grid_for(rp, 8, p.sm_count)), dim3(256), 0, stream,
-                   static_cast<const uint4*>(p.x), static_cast<const uint4*>(p.dout),
-                   static_cast<const int32_t*>(p.pperm), static_cast<const int32_t*>(p.pmt), E, p.K, D / 8,
-                   static_cast<uint4*>(p.xpp), static_cast<uint4*>(p.dop)) != cudaSuccess)
+        launch_pdl(k_gather_bwd, dim3(grid_for(rp + p.T * ceil_div(D / 8, kGatherChunkVec), 8, p.sm_count)),
+                   dim3(256), 0, stream, static_cast<const uint4*>(p.x), static_cast<const uint4*>(p.dout),
+                   static_cast<const int32_t*>(p.pperm), static_cast<const int32_t*>(p.pinv),
+                   static_cast<const int32_t*>(p.pmt), E, p.K, p.T, D / 8, static_cast<uint4*>(p.xpp),
+                   static_cast<uint4*>(p.dop)) != cudaSuccess)
         return MOE_ERR_CUDA;
 
     GemmArgs a{};

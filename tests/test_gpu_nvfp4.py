@@ -172,6 +172,8 @@ CASES = {
     "k1": (129, 128, 256, 3, 1, "uniform"),
     "t1": (1, 256, 128, 8, 4, "uniform"),
     "k_equals_e": (40, 128, 128, 8, 8, "uniform"),
+    "k_over_32": (24, 256, 128, 48, 40, "uniform"),  # a token's destination rows in two groups of lanes
+    "max_experts": (64, 128, 128, 4096, 4, "uniform"),  # E at its maximum, almost every expert empty
     "skewed_small": (256, 256, 384, 16, 4, "zipf"),
 }
 
@@ -187,8 +189,9 @@ def test_nvfp4_forward_matches_oracle(name):
     assert err <= OUT_TOL, (name, err)
 
 
-def test_activation_rows_bit_exact_and_padding_scales_zero():
-    T, D, F, E, K = 300, 640, 256, 6, 3  # D leaves two padding scale groups per row
+@pytest.mark.parametrize("T", [300, 2100])  # 1024-column work items, and whole rows (T >= 2048)
+def test_activation_rows_bit_exact_and_padding_scales_zero(T):
+    D, F, E, K = 640, 256, 6, 3  # D leaves two padding scale groups per row
     d = problem(T, D, F, E, K, seed=4)
     out, ws = run_nv(d)
     lay = binding.moe_nvfp4_workspace_layout(T, D, F, E, K)

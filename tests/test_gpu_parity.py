@@ -38,6 +38,8 @@ CASES = {
     "k1": (129, 128, 256, 3, 1, "uniform"),
     "t1": (1, 256, 128, 8, 4, "uniform"),
     "k_equals_e": (40, 128, 128, 8, 8, "uniform"),
+    "k_over_32": (24, 256, 128, 48, 40, "uniform"),  # a token's destination rows in two groups of lanes
+    "max_experts": (64, 128, 128, 4096, 4, "uniform"),  # E at its maximum, almost every expert empty
     "skew": (400, 128, 192, 16, 4, "zipf"),
 }
 

@@ -39,6 +39,9 @@
 //   static constexpr bool kCooperative = true
 //        launch as a cooperative grid (every CTA resident at once), required when acquire()
 //        waits for tiles other CTAs own.
+//   __device__ static uint32_t idesc(const Tile&), tx_bytes(const Tile&)
+//        per-tile instruction descriptor and stage transaction bytes, for policies whose tiles
+//        differ in N (default: kIdesc and the shape's kTxBytes)
 //   static constexpr bool kDynamicSchedule = true
 //        CTAs take tiles in list order from the global counter args.ticket (zero on entry)
 //        instead of the fixed c, c + grid, ...: the producer takes a tile and hands its index to
@@ -149,7 +152,7 @@ constexpr int kStageRowU4 = 9;  // 144-byte row stride in 16-byte units
 constexpr int kEpilogueStagingBytes = (kEpilogueThreads / 32) * 32 * kStageRowU4 * 16;
 
 constexpr int kTileRing = 4;  // tiles in flight between producer and consumers (dynamic schedule)
-constexpr int kTileStoreBytes = 32;
+constexpr int kTileStoreBytes = 48;
 
 struct alignas(16) PipeState {
     uint64_t full[kMaxStages];
@@ -216,6 +219,13 @@ template <class P>
 struct HasAcquire<P, std::void_t<decltype(P::acquire(std::declval<const typename P::Tile&>(),
                                                        std::declval<const GemmArgs&>(),
                                                        std::declval<volatile int*>()))>> : std::true_type {};
+
+template <class P, class = void>
+struct HasTileShape : std::false_type {};
+template <class P>
+struct HasTileShape<P, std::void_t<decltype(P::idesc(std::declval<const typename P::Tile&>())),
+                                   decltype(P::tx_bytes(std::declval<const typename P::Tile&>()))>>
+    : std::true_type {};
 
 template <class P, class = void>
 struct IsDynamic : std::false_type {};
@@ -439,7 +449,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     uint8_t* sa = smem + s * S::kStageBytes;
-                    mbar_arrive_expect_tx(&ps->full[s], S::kTxBytes);
+                    if constexpr (HasTileShape<P>::value) mbar_arrive_expect_tx(&ps->full[s], P::tx_bytes(t));
+                    else mbar_arrive_expect_tx(&ps->full[s], S::kTxBytes);
                     if constexpr (S::kBlockScaled)
                         P::load(t, kb, sa, sa + S::kABytes, sa + S::kABytes + S::kBBytes, &ps->full[s], tmap_a,
                                 tmap_b, args);
@@ -497,6 +508,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tcgen05_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * S::kAccCols;
+                uint32_t idesc = P::kIdesc;
+                if constexpr (HasTileShape<P>::value) idesc = P::idesc(t);
                 for (int32_t kb = 0; kb < t.kblocks; ++kb, ++it) {
                     const uint32_t s = it % S::kStages;
                     const uint32_t ph = (it / S::kStages) & 1u;
@@ -521,12 +534,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)  // 128-byte stage rows, 32 bytes of K per MMA
                             S::mma(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
-                                   P::kIdesc, slot, kk, (kb | kk) != 0 ? 1u : 0u);
+                                   idesc, slot, kk, (kb | kk) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
                             mma_bf16_ss(d_tmem, operand_desc<P::kAMnMajor>(a0, kk),
-                                        operand_desc<P::kBMnMajor>(b0, kk), P::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                                        operand_desc<P::kBMnMajor>(b0, kk), idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit(&ps->empty[s]);  // frees the stage once these MMAs have read it
                     if (!decoded) {

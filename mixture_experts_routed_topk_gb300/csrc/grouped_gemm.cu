@@ -28,6 +28,7 @@ namespace {
 
 struct RowTile {
     int32_t e, n, row0, rows, kblocks;
+    int32_t f0, nf;  // gate/up tiles: the first f value and the f values (128, or 64 / 32 in the tail)
 };
 
 // Tile index -> (expert, column tile, first routed row, valid rows) for the forward tile list:
@@ -47,34 +48,74 @@ __device__ __forceinline__ RowTile decode_row_tile(int32_t tile, const GemmArgs&
 }
 
 // Gate/up GEMM with SwiGLU: A = XP rows (K-major, K = D), B = w13 gate and up rows (K-major).
+//
+// Tail split: the tiles past the last whole wave of the grid are cut along f into halves (64 gate +
+// 64 up columns, N = 128) or quarters (N = 64) when that many pieces still fit in one wave, so the
+// last wave takes a half or a quarter of a tile's time instead of a whole one on a few SMs. The B
+// boxes of the pieces come from tensor maps with 64- and 32-row boxes (maps 2 and 3). Every output
+// element is still one K-ordered sum of the same products.
 struct FwdGateUp {
     using Tile = RowTile;
     static constexpr bool kAMnMajor = false, kBMnMajor = false;
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBRows);
 
-    __device__ static int32_t num_tiles(const GemmArgs& a) { return __ldg(a.tiles + a.E); }
-    __device__ static Tile decode(int32_t tile, const GemmArgs& a) { return decode_row_tile(tile, a); }
+    // tiles in whole waves, and how many pieces each tile of the partial last wave becomes
+    __device__ static void tail(int32_t total, int32_t& full, int32_t& split) {
+        const int32_t grid = static_cast<int32_t>(gridDim.x);
+        const int32_t rem = total % grid;
+        full = total - rem;
+        split = 4 * rem <= grid ? 4 : (2 * rem <= grid ? 2 : 1);
+    }
+
+    __device__ static int32_t num_tiles(const GemmArgs& a) {
+        const int32_t total = __ldg(a.tiles + a.E);
+        int32_t full, split;
+        tail(total, full, split);
+        return full + (total - full) * split;
+    }
+    __device__ static Tile decode(int32_t tile, const GemmArgs& a) {
+        int32_t full, split;
+        tail(__ldg(a.tiles + a.E), full, split);
+        if (tile < full) {
+            Tile t = decode_row_tile(tile, a);
+            t.f0 = t.n * kBN1;
+            t.nf = kBN1;
+            return t;
+        }
+        const int32_t j = tile - full;
+        Tile t = decode_row_tile(full + j / split, a);
+        t.nf = kBN1 / split;
+        t.f0 = t.n * kBN1 + (j % split) * t.nf;
+        return t;
+    }
+    __device__ static uint32_t idesc(const Tile& t) {
+        return t.nf == kBN1 ? kIdesc : (t.nf == kBN1 / 2 ? idesc_bf16_f32(kBM, kBN1) : idesc_bf16_f32(kBM, kBN1 / 2));
+    }
+    __device__ static uint32_t tx_bytes(const Tile& t) {
+        return static_cast<uint32_t>(kABytes + 2 * t.nf * kBK * 2);
+    }
 
     __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
                                 const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs& a) {
-        const int32_t gate = t.e * 2 * a.F + t.n * kBN1;
+        const CUtensorMap* mb = t.nf == kBN1 ? tb : (t.nf == kBN1 / 2 ? ta + 2 : ta + 3);
+        const int32_t gate = t.e * 2 * a.F + t.f0;
         tma_load_2d(sa, ta, bar, kb * kBK, t.row0);
-        tma_load_2d(sb, tb, bar, kb * kBK, gate);
-        tma_load_2d(sb + kBBytes / 2, tb, bar, kb * kBK, gate + a.F);
+        tma_load_2d(sb, mb, bar, kb * kBK, gate);
+        tma_load_2d(sb + t.nf * kBK * 2, mb, bar, kb * kBK, gate + a.F);
     }
 
     __device__ static void epilogue(const Tile& t, uint32_t taddr, int row_in_tile, uint4*, const GemmArgs& a) {
         const bool valid = row_in_tile < t.rows;
         const int64_t row = static_cast<int64_t>(t.row0) + row_in_tile;
 #pragma unroll 1
-        for (int c = 0; c < kBN1 / 32; ++c) {
+        for (int c = 0; c < t.nf / 32; ++c) {
             __syncwarp();  // tcgen05.ld is .sync.aligned: reconverge after the masked store
             uint32_t g[32], u[32];
             tmem_ld_32cols(taddr + c * 32, g);
-            tmem_ld_32cols(taddr + kBN1 + c * 32, u);
+            tmem_ld_32cols(taddr + t.nf + c * 32, u);
             tmem_ld_wait(g);
             tmem_ld_tie(u);
-            const int32_t f0 = t.n * kBN1 + c * 32;
+            const int32_t f0 = t.f0 + c * 32;
             if (valid && f0 < a.F) {
                 uint32_t packed[16];
 #pragma unroll
@@ -239,6 +280,8 @@ struct FwdMega {
         t.rows = min(kBM, ne - m * kBM);
         t.kblocks = t.phase ? a.kblocks_b : a.kblocks;
         t.rt = __ldg(a.tiles + t.e) / a.ntn + m;
+        t.f0 = t.n * kBN1;  // gate/up tiles are never split here
+        t.nf = kBN1;
         return t;
     }
 
@@ -356,13 +399,16 @@ int sm_count_grid(int64_t max_tiles, int sm_count) {
 
 moe_status_t launch_gemm1_swiglu(const GemmProblem& p, const void* xp, const void* w13, void* h,
                                  cudaStream_t stream) {
-    CUtensorMap ta, tb;
-    if (!make_tmap(&ta, xp, static_cast<uint64_t>(p.D), static_cast<uint64_t>(p.R), kBK, kBM) ||
-        !make_tmap(&tb, w13, static_cast<uint64_t>(p.D), static_cast<uint64_t>(p.E) * 2 * p.F, kBK, kBN1))
+    GemmMaps maps{};
+    const uint64_t w13_rows = static_cast<uint64_t>(p.E) * 2 * p.F;
+    if (!make_tmap(&maps.m[0], xp, static_cast<uint64_t>(p.D), static_cast<uint64_t>(p.R), kBK, kBM) ||
+        !make_tmap(&maps.m[1], w13, static_cast<uint64_t>(p.D), w13_rows, kBK, kBN1) ||
+        !make_tmap(&maps.m[2], w13, static_cast<uint64_t>(p.D), w13_rows, kBK, kBN1 / 2) ||  // tail halves
+        !make_tmap(&maps.m[3], w13, static_cast<uint64_t>(p.D), w13_rows, kBK, kBN1 / 4))    // tail quarters
         return MOE_ERR_CUDA;
     GemmArgs a = row_args(p, p.D / kBK);
     a.out0 = static_cast<__nv_bfloat16*>(h);
-    return launch_gemm<FwdGateUp>(ta, tb, a, row_grid(p, static_cast<int32_t>(ceil_div(p.F, kBN1))), stream);
+    return launch_gemm<FwdGateUp>(maps, a, row_grid(p, static_cast<int32_t>(ceil_div(p.F, kBN1))), stream);
 }
 
 moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void* w2, const int32_t* perm,

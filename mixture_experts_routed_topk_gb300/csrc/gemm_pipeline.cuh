@@ -1,12 +1,14 @@
 // gemm_pipeline.cuh -- the persistent, warp-specialised tcgen05 GEMM pipeline shared by every
 // grouped GEMM of the library (forward and backward), generic over a tile policy.
 //
-// One CTA per SM walks tiles c, c + grid, ... of a tile list the policy defines. Warp 0 issues TMA
-// loads into a shared-memory ring of stages, warp 1 owns all 512 TMEM columns and issues
-// tcgen05.mma from one thread into one of two fp32 accumulators, warps 2-5 run the policy's
-// epilogue from TMEM (one TMEM lane = one output row per thread). full/empty mbarriers link
-// producer and MMA; acc_full/acc_empty link MMA and epilogue, so a tile's epilogue overlaps the
-// next tile's mainloop. Every wait is bounded.
+// One CTA per SM walks tiles c, c + grid, ... of a tile list the policy defines (or claims them in
+// list order from a global counter, see kDynamicSchedule). Warp 0 issues TMA loads into a
+// shared-memory ring of stages, warp 1 owns all 512 TMEM columns and issues tcgen05.mma from one
+// thread into one of two fp32 accumulators, warps 2-5 run the policy's epilogue from TMEM (one
+// TMEM lane = one output row per thread). full/empty mbarriers link producer and MMA;
+// acc_full/acc_empty link MMA and epilogue, so a tile's epilogue overlaps the next tile's
+// mainloop. The producer and the MMA thread decode the next tile while the current one's first
+// stage is in flight, so no decode sits between two tiles' MMAs. Every wait is bounded.
 //
 // The policy's Shape fixes the ring and the MMA kind (Bf16Shape unless the policy names another):
 //   Bf16Shape: 4 stages of 16 KB A + 32 KB B (64 bf16 of K), 128 x 256 accumulators, kind::f16.
@@ -30,23 +32,23 @@
 //        (block-scaled shapes: load(t, kb, sa, sb, sf, bar, ta, tb, args), sf = the scale chunks)
 //   __device__ static void epilogue(const Tile&, uint32_t taddr, int row, uint4* stage,
 //                                   const GemmArgs&)          (taddr = this warp's TMEM lanes)
-// Every load() must deliver exactly the shape's kTxBytes into the stage. ta and tb point into the
+// Every load() must deliver exactly the shape's kTxBytes (or tx_bytes(t)) into the stage. ta and tb point into the
 // kernel's array of four tensor maps (tb == ta + 1); a policy with more operands reads ta[2], ta[3].
 // Optional:
 //   __device__ static bool acquire(const Tile&, const GemmArgs&, volatile int* abort)
 //        run by the producer before a tile's first load: waits (bounded) until data that other
 //        CTAs of the same grid produce for this tile is visible to TMA; false aborts the CTA.
 //   static constexpr bool kCooperative = true
-//        launch as a cooperative grid (every CTA resident at once), required when acquire()
-//        waits for tiles other CTAs own.
+//        launch as a cooperative grid (every CTA resident at once), so that a CTA waiting in
+//        acquire() for tiles other CTAs own never waits for a CTA that has not started.
 //   __device__ static uint32_t idesc(const Tile&), tx_bytes(const Tile&)
 //        per-tile instruction descriptor and stage transaction bytes, for policies whose tiles
 //        differ in N (default: kIdesc and the shape's kTxBytes)
 //   static constexpr bool kDynamicSchedule = true
 //        CTAs take tiles in list order from the global counter args.ticket (zero on entry)
-//        instead of the fixed c, c + grid, ...: the producer takes a tile and hands its index to
-//        the MMA and epilogue warps through a small ring of shared-memory slots. For tile lists of
-//        unequal tiles, where a fixed assignment lets CTAs drift apart along the list.
+//        instead of the fixed c, c + grid, ...: the producer takes a tile, decodes it and hands it
+//        to the MMA and epilogue warps through a small ring of shared-memory slots. For tile lists
+//        of unequal tiles, where a fixed assignment lets CTAs drift apart along the list.
 #pragma once
 
 #include <cuda.h>

@@ -20,18 +20,21 @@ from mixture_experts_routed_topk_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def sample_pairs(routing: dict, rng, per_expert=6) -> np.ndarray:
+def sample_pairs(routing: dict, rng, per_extreme=64, per_random=6) -> np.ndarray:
+    """Up to 64 pairs each of the hottest and the coldest non-empty expert, 6 each of two random
+    experts, always with the first and last row of every sampled segment (tile edges)."""
     counts, offsets, perm = routing["counts"], routing["offsets"], routing["perm"]
     nonempty = np.flatnonzero(counts)
     hot = int(np.argmax(counts))
     cold = int(nonempty[np.argmin(counts[nonempty])])
-    picks = {hot, cold, *rng.choice(nonempty, size=min(2, nonempty.size), replace=False).tolist()}
+    picks = {e: per_random for e in rng.choice(nonempty, size=min(2, nonempty.size), replace=False).tolist()}
+    picks[hot] = picks[cold] = per_extreme
     rows = []
     for e in sorted(picks):
         a, b = int(offsets[e]), int(offsets[e + 1])
         chosen = {a, b - 1}
         if b - a > 2:
-            chosen.update(rng.integers(a, b, size=min(per_expert - 2, b - a)).tolist())
+            chosen.update(rng.choice(np.arange(a + 1, b - 1), size=min(picks[e] - 2, b - a - 2), replace=False).tolist())
         rows.extend(sorted(chosen))
     return perm[np.asarray(rows, dtype=np.int64)].astype(np.int64)
 

@@ -162,6 +162,14 @@ def path_costs(T, D, F, E, K, touched, wbytes=2.0):
     return 6 * T * K * D * F, touched * 3 * F * D * wbytes + 2 * T * D * 2 + T * K * 8
 
 
+def overhead_bytes(T, D, F, K, q=2.0):
+    """The implementation's intermediate round trips (written, then read back), which the
+    algorithmic bytes leave out: the routed rows of x (XP, or XQ at q bytes per element), the SwiGLU
+    output (H / HQ) and the bf16 score-weighted pair outputs (Y)."""
+    R = T * K
+    return {"xp": 2 * R * D * q, "h": 2 * R * F * q, "y": 2 * R * D * 2}
+
+
 def roofline_entry(name, costs, seconds, peaks, sustained, traffic, tensor_scale=1.0):
     """tensor_scale multiplies the measured bf16 peak for another operand type (PRECISIONS)."""
     c = costs[name]
@@ -597,7 +605,8 @@ def run_ours(args, rank, world, local_rank):
                 "l2": "flushed between steps (512 MB write)", "seed": args.seed},
         tflops=round(world * flops / step_s / 1e12, 2),
         path_roofline={"ms": round(t_roof * 1e3, 4), "frac": round(t_roof / step_s, 4),
-                       "flops": flops, "alg_bytes": alg_bytes},
+                       "flops": flops, "alg_bytes": alg_bytes,
+                       "overhead_bytes": {k: int(v) for k, v in overhead_bytes(T, D, F, K, prec["elem_bytes"]).items()}},
         roofline=roof,
         stage_ms={s: round(v, 4) for s, v in mean_stage.items()},
         e2e={"value": round(world * T * args.steps / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,

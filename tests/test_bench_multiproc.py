@@ -73,3 +73,11 @@ def test_roofline_arithmetic():
     flops, nbytes = bench.path_costs(4096, 2048, 1408, 64, 6, 64)
     assert flops == 6 * 4096 * 6 * 2048 * 1408
     assert nbytes == 64 * 3 * 1408 * 2048 * 2 + 2 * 4096 * 2048 * 2 + 4096 * 6 * 8
+    # the intermediates' round trips reported beside the result (large workload: 3.76 / 1.07 /
+    # 3.76 GB for XP, H and Y)
+    ov = bench.overhead_bytes(16384, 7168, 2048, 8)
+    assert ov == {"xp": 2 * 131072 * 7168 * 2, "h": 2 * 131072 * 2048 * 2, "y": 2 * 131072 * 7168 * 2}
+    assert abs(ov["xp"] / 1e9 - 3.76) < 0.01 and abs(ov["h"] / 1e9 - 1.07) < 0.01
+    # fused GEMMs: 6 R D F flops, H stays inside the kernel
+    fused = costs["fused_gemms"]
+    assert fused["flops"] == costs["gemm1_swiglu"]["flops"] + costs["gemm2_score"]["flops"]

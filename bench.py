@@ -8,7 +8,7 @@ weighting, and the combine -- through the C ABI, on inputs already resident in H
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
                     [--precision bf16|mxfp8|nvfp4] [--pass fwd|bwd] [--pipeline staged|mega]
 
---pipeline mega runs the bf16 forward with both grouped GEMMs fused into one cooperative grid
+--pipeline mega runs the bf16 forward with both grouped GEMMs fused into one grid
 (dispatch, fused GEMMs, combine); the default runs them as separate kernels.
 
 --precision mxfp8 / nvfp4 runs a block-scaled forward (E4M3 operands with UE8M0 scales per 32, or

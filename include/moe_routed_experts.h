@@ -181,7 +181,7 @@ moe_status_t moe_routed_experts_fwd_rmsnorm(const void *x, const int32_t *topk_i
 /*
  * The forward pass with the two grouped GEMMs fused into one pipeline (Dist-MoE 0.1.0,
  * "Block-scaled execution": the Mega pipeline runs both projections as one chunked pipeline, with
- * the staged pipeline's tensor and memory contracts). One cooperative grid walks the gate/up
+ * the staged pipeline's tensor and memory contracts). One grid walks the gate/up
  * tiles of expert e and the down tiles of an earlier expert in turn; a down tile starts once the
  * gate/up tiles of its 128 rows have written their H rows, so H is read back from L2 and the two
  * GEMMs share one launch and one tail. The tiles and roundings are those of
@@ -191,9 +191,9 @@ moe_status_t moe_routed_experts_fwd_rmsnorm(const void *x, const int32_t *topk_i
  *   workspace    device, moe_mega_workspace_bytes(T, D, F, E, K) bytes (it adds the READY
  *                counters and a Y region that may not overlap XP, because Y rows are written
  *                while later experts' XP rows are still being read)
- * Errors as for moe_routed_experts_fwd; MOE_ERR_CUDA also when the device cannot hold the grid
- * as one cooperative launch (never on a whole GB300). A row tile whose H never arrives ends the
- * kernel through its bounded wait with MOE_DEV_TIMEOUT.
+ * Errors as for moe_routed_experts_fwd. A row tile whose H never arrives ends the kernel through
+ * its bounded wait with MOE_DEV_TIMEOUT. Calls on different workspaces may run at once on
+ * different streams.
  */
 moe_status_t moe_routed_experts_fwd_mega(const void *x, const int32_t *topk_ids, const void *topk_scores,
                                          int32_t scores_dtype, const void *w13, const void *w2, void *out,

@@ -38,9 +38,8 @@
 //   __device__ static bool acquire(const Tile&, const GemmArgs&, volatile int* abort)
 //        run by the producer before a tile's first load: waits (bounded) until data that other
 //        CTAs of the same grid produce for this tile is visible to TMA; false aborts the CTA.
-//   static constexpr bool kCooperative = true
-//        launch as a cooperative grid (every CTA resident at once), so that a CTA waiting in
-//        acquire() for tiles other CTAs own never waits for a CTA that has not started.
+//        Requires kDynamicSchedule and a list whose tiles depend only on earlier tiles: then only
+//        running CTAs hold tiles, so the wait never depends on a CTA that has not started.
 //   __device__ static uint32_t idesc(const Tile&), tx_bytes(const Tile&)
 //        per-tile instruction descriptor and stage transaction bytes, for policies whose tiles
 //        differ in N (default: kIdesc and the shape's kTxBytes)
@@ -234,10 +233,6 @@ struct IsDynamic : std::false_type {};
 template <class P>
 struct IsDynamic<P, std::void_t<decltype(P::kDynamicSchedule)>> : std::integral_constant<bool, P::kDynamicSchedule> {};
 
-template <class P, class = void>
-struct IsCooperative : std::false_type {};
-template <class P>
-struct IsCooperative<P, std::void_t<decltype(P::kCooperative)>> : std::integral_constant<bool, P::kCooperative> {};
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -398,6 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = ps->tmem_base;
     const int32_t total = P::num_tiles(args);
     constexpr bool kDynamic = IsDynamic<P>::value;
+    static_assert(!HasAcquire<P>::value || kDynamic, "a tile that waits for other tiles needs the dynamic schedule");
     static_assert(!kDynamic || (sizeof(typename P::Tile) <= kTileStoreBytes &&
                                 std::is_trivially_copyable<typename P::Tile>::value),
                   "a dynamically scheduled policy's tiles travel through the shared-memory ring");
@@ -629,26 +625,10 @@ moe_status_t launch_gemm(const GemmMaps& maps, const GemmArgs& a, int grid, cuda
             return MOE_ERR_CUDA;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    if constexpr (IsCooperative<P>::value) {
-        // every CTA resident at once (one per SM at this shared-memory size), so a CTA that waits
-        // for another CTA's tile never waits for one that has not started
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kGemmThreads);
-        cfg.dynamicSmemBytes = kGemmSmemBytes;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_grouped_gemm<P>, maps, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-    } else {
-        return launch_pdl(k_grouped_gemm<P>, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, stream, maps, a) ==
-                       cudaSuccess
-                   ? MOE_OK
-                   : MOE_ERR_CUDA;
-    }
+    return launch_pdl(k_grouped_gemm<P>, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, stream, maps, a) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 template <class P>

@@ -193,7 +193,7 @@ struct FwdDownT {
 
 // ------------------------------------------------------------------ the fused (Mega) forward
 //
-// Both GEMMs in one cooperative grid (Dist-MoE 0.1.0, "Block-scaled execution": the Mega pipeline
+// Both GEMMs in one grid (Dist-MoE 0.1.0, "Block-scaled execution": the Mega pipeline
 // runs the two projections as one chunked pipeline instead of separate W13 and SwiGLU/W2 kernels).
 // The grid walks one interleaved list of slots: a slot is one expert's gate/up tiles (phase 0) or
 // its down tiles (phase 1); expert e's down slot comes after the gate/up slot of expert e + L, so
@@ -203,8 +203,8 @@ struct FwdDownT {
 // from a global counter (the tiles differ in length, so a fixed assignment would let CTAs drift
 // apart along the list). A down tile's producer waits (bounded) until the four epilogue warps of
 // every gate/up tile of its row tile have released the row tile's counter; those tiles come
-// earlier in the list and were claimed by running CTAs, so the lowest unfinished tile can always
-// proceed. The tiles, their arithmetic and their roundings are
+// earlier in the list and only running CTAs claim tiles, so the lowest unfinished tile can always
+// proceed, whether or not every CTA of the grid is resident (another stream may hold SMs). The tiles, their arithmetic and their roundings are
 // the staged kernels', so the result is bit-identical to the staged forward's.
 
 struct MegaTile : RowTile {
@@ -240,7 +240,6 @@ struct FwdMega {
     using Tile = MegaTile;
     static constexpr bool kAMnMajor = false, kBMnMajor = false;
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBRows);
-    static constexpr bool kCooperative = true;
     static constexpr bool kDynamicSchedule = true;  // gate/up and down tiles differ in length
     static_assert(FwdGateUp::kIdesc == kIdesc && FwdDownT<false>::kIdesc == kIdesc, "one accumulator shape");
 

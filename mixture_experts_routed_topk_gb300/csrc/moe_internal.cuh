@@ -114,7 +114,7 @@ moe_status_t launch_gemm2_score(const GemmProblem& p, const void* h, const void*
                                 const void* scores, int32_t scores_dtype, void* y, float* rms_sumsq,
                                 cudaStream_t stream);
 
-// The fused forward: both grouped GEMMs in one cooperative grid, the down tiles of a row tile
+// The fused forward: both grouped GEMMs in one grid, the down tiles of a row tile
 // starting once its gate/up tiles have written their H rows. ready: the grid's tile counter, then
 // from word 32 on one uint32 per row tile (ceil(R/128) + min(R, E) of them), all zero on entry. y must not overlap xp (Y rows are written while
 // later experts' XP rows are still being read).

@@ -21,14 +21,19 @@ def problem(T, D, F, E, K, seed):
     return to_device(d)
 
 
-def test_concurrent_calls_on_separate_workspaces():
-    T, D, F, E, K = 512, 512, 384, 8, 4
+@pytest.mark.parametrize("entry", ["staged", "mega"])
+def test_concurrent_calls_on_separate_workspaces(entry):
+    # mega: two fused grids share the SMs; a grid's down tiles wait only for tiles its own running
+    # CTAs claimed, so each finishes whatever the other holds
+    T, D, F, E, K = (512, 512, 384, 8, 4) if entry == "staged" else (2048, 256, 1024, 32, 6)
+    fwd = binding.moe_routed_experts_fwd if entry == "staged" else binding.moe_routed_experts_fwd_mega
+    nbytes = (binding.moe_workspace_bytes if entry == "staged" else binding.moe_mega_workspace_bytes)(T, D, F, E, K)
     probs = [problem(T, D, F, E, K, seed) for seed in (21, 22)]
-    wss = [binding.alloc_workspace(binding.moe_workspace_bytes(T, D, F, E, K)) for _ in probs]
+    wss = [binding.alloc_workspace(nbytes) for _ in probs]
     alone = []
     for d, ws in zip(probs, wss):
         out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
-        binding.moe_routed_experts_fwd(d["x"], d["topk_ids"], d["topk_scores"], d["w13"], d["w2"], out, ws)
+        fwd(d["x"], d["topk_ids"], d["topk_scores"], d["w13"], d["w2"], out, ws)
         alone.append(out)
     torch.cuda.synchronize()
     streams = [torch.cuda.Stream() for _ in probs]
@@ -40,8 +45,8 @@ def test_concurrent_calls_on_separate_workspaces():
             d = probs[i]
             with torch.cuda.stream(streams[i]):
                 for _ in range(5):
-                    binding.moe_routed_experts_fwd(d["x"], d["topk_ids"], d["topk_scores"], d["w13"], d["w2"],
-                                                   outs[i], wss[i], stream=streams[i])
+                    fwd(d["x"], d["topk_ids"], d["topk_scores"], d["w13"], d["w2"], outs[i], wss[i],
+                        stream=streams[i])
         except Exception as exc:  # surfaced below, on the main thread
             errors.append(exc)
 

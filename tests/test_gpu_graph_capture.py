@@ -30,7 +30,7 @@ def test_forward_replays_from_a_cuda_graph(precision):
     if precision == "bf16":
         ws = binding.alloc_workspace(binding.moe_workspace_bytes(T, D, F, E, K))
         call = lambda s: binding.moe_routed_experts_fwd(x, ids, sc, d["w13"], d["w2"], out, ws, stream=s)
-    elif precision == "mega":  # the fused forward: a cooperative launch inside the graph
+    elif precision == "mega":  # the fused forward: one dynamically scheduled grid for both GEMMs
         ws = binding.alloc_workspace(binding.moe_mega_workspace_bytes(T, D, F, E, K))
         call = lambda s: binding.moe_routed_experts_fwd_mega(x, ids, sc, d["w13"], d["w2"], out, ws, stream=s)
     elif precision == "mxfp8":

@@ -1,4 +1,4 @@
-"""The fused (Mega) forward on the GPU: one cooperative grid runs the gate/up and down grouped GEMMs,
+"""The fused (Mega) forward on the GPU: one grid runs the gate/up and down grouped GEMMs,
 a down tile starting once the gate/up tiles of its rows have written H. It computes the same tiles
 with the same roundings as the staged forward, so its output must be bit-identical to the staged
 one (and therefore within the oracle tolerance) on every case: ragged tails, empty experts,

@@ -70,6 +70,8 @@ CASES = {
     "empty_experts": (20, 128, 128, 64, 2, "uniform"),  # most experts get no rows: zero dW
     "k1": (129, 128, 256, 3, 1, "uniform"),
     "skew": (400, 128, 192, 16, 4, "zipf"),
+    "k_over_32": (24, 128, 128, 48, 40, "uniform"),  # 40 padded rows per token in the gather
+    "max_experts": (48, 64, 64, 4096, 4, "uniform"),  # E at its maximum: almost every dW block zero
 }
 
 

@@ -81,3 +81,21 @@ def test_roofline_arithmetic():
     # fused GEMMs: 6 R D F flops, H stays inside the kernel
     fused = costs["fused_gemms"]
     assert fused["flops"] == costs["gemm1_swiglu"]["flops"] + costs["gemm2_score"]["flops"]
+
+
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8", "nvfp4"])
+def test_reference_arm_line(precision):
+    # the reference arm times the CPU oracle; on the tiny workload it needs no GPU and ends in seconds
+    import subprocess
+
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--precision", precision, "--steps", "2", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["value"] > 0 and line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "tiny" and line["config"]["precision"] == precision

@@ -40,6 +40,10 @@ CASES = {
     "k_equals_e": (40, 128, 128, 8, 8, "uniform"),
     "k_over_32": (24, 256, 128, 48, 40, "uniform"),  # a token's destination rows in two groups of lanes
     "max_experts": (64, 128, 128, 4096, 4, "uniform"),  # E at its maximum, almost every expert empty
+    # one row tile per expert and 8 gate/up column tiles: 184 (200) tiles on a 152-SM grid leave a
+    # partial wave of 32 (48) tiles, which the gate/up GEMM splits into quarters (halves)
+    "tail_quarters": (2000, 128, 1024, 23, 1, "uniform"),
+    "tail_halves": (2000, 128, 1024, 25, 1, "uniform"),
     "skew": (400, 128, 192, 16, 4, "zipf"),
 }
 

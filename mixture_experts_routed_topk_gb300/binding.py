@@ -253,6 +253,8 @@ def moe_fwd_mega_stages(x, topk_ids, topk_scores, w13, w2, out, workspace, stage
     _need(out, "out", torch.bfloat16, 2)
     _need(workspace, "workspace", torch.uint8)
     T, D, F, E, K = _dims(x, topk_ids, w13)
+    if tuple(w2.shape) != (E, D, F) or tuple(out.shape) != (T, D) or tuple(topk_scores.shape) != (T, K):
+        raise ValueError("inconsistent shapes among w2 [E,D,F], out [T,D], topk_scores [T,K]")
     sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
     _check("moe_fwd_mega_stages", load().moe_fwd_mega_stages(
         _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(out),

@@ -5,8 +5,15 @@ One step = one pass of the whole path over one batch: routing (histogram, scan, 
 row gather), the gate/up grouped GEMM with SwiGLU, the down grouped GEMM with the score
 weighting, and the combine -- through the C ABI, on inputs already resident in HBM.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
-                    [--precision bf16|mxfp8|nvfp4] [--pass fwd|bwd] [--pipeline staged|mega]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--also NAMES]
+                    [--impl ours|reference] [--precision bf16|mxfp8|nvfp4] [--pass fwd|bwd]
+                    [--pipeline staged|mega]
+
+The line's workload is --config (default: large, T=16384 D=7168 F=2048 E=256 K=8, the largest
+single-GPU workload and the compute-bound target). The workloads named by --also (default: decode,
+the weight-streaming target at T=64 on the same weights, and medium) are measured the same way after
+it and reported in the same line, each as a sub-record under its own name with its own timing, stage
+times, rooflines, end-to-end rate, clocks and CPU baseline.
 
 --pipeline mega runs the bf16 forward with both grouped GEMMs fused into one grid
 (dispatch, fused GEMMs, combine); the default runs them as separate kernels.
@@ -68,7 +75,11 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=500)
     p.add_argument("--warmup", type=int, default=10)
-    p.add_argument("--config", default="medium", choices=["tiny", "medium", "decode", "large", "skewed"])
+    p.add_argument("--config", default="large", choices=["tiny", "medium", "decode", "large", "skewed"],
+                   help="the workload of the line (default: large, the largest single-GPU workload)")
+    p.add_argument("--also", default="decode,medium",
+                   help="comma-separated workloads measured after --config and reported as sub-records of "
+                        "the same line, each under its own name (empty: none)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--precision", default="bf16", choices=sorted(PRECISIONS),
                    help="forward operands: bf16, MXFP8 E4M3 or NVFP4 E2M1 (block-scaled, prepared weights)")
@@ -78,9 +89,13 @@ def parse_args(argv=None):
                    help="bf16 forward: separate GEMM kernels (staged) or both GEMMs in one grid (mega)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--tokens", type=int, default=None,
-                   help="replace the workload's T (smaller cases for profiling runs)")
+                   help="replace the workload's T (smaller cases for profiling runs; no sub-records)")
+    p.add_argument("--experts", type=int, default=None,
+                   help="replace the workload's E (a weight-streaming case small enough for ncu; no sub-records)")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host cores")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    p.add_argument("--sub-cpu-seconds", type=float, default=8.0,
+                   help="target CPU time of the oracle sample of each sub-record")
     return p.parse_args(argv)
 
 
@@ -204,19 +219,31 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config: str, kernel: str):
+def recorded_traffic(config: str, kernel: str, touched: int | None = None):
     """DRAM bytes per launch recorded by an ncu capture (profiles/dram_traffic.md), or None when
-    absent or taken on other kernel sources."""
+    absent or taken on other kernel sources.
+
+    A row's config is a workload name, or a name with its expert count cut for the capture
+    ("decode (E=16)"): a weight-streaming kernel on a workload too large to capture under ncu is
+    captured with fewer experts, and its traffic, which grows with the experts it touches, is scaled
+    to `touched` experts by the ratio of touched experts (the row's last numeric column)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     src = kernel_source_hash()
-    for m in re.finditer(r"^\|\s*(\w+)\s*\|\s*(\w+)\s*\|\s*([0-9a-f]{16})\s*\|\s*([0-9.eE+]+)\s*\|", text, re.M):
-        if m.group(1) == config and m.group(2) == kernel and m.group(3) == src:
-            return float(m.group(4))
-    return None
+    row = re.compile(r"^\|\s*(\w+)(?:\s*\(E=(\d+)\))?\s*\|\s*(\w+)\s*\|\s*([0-9a-f]{16})\s*\|\s*([0-9.eE+]+)\s*\|"
+                     r"\s*[0-9.eE+]+\s*\|\s*[0-9.eE+]+\s*\|\s*(\d+)\s*\|", re.M)
+    scaled = None
+    for m in row.finditer(text):
+        if m.group(1) != config or m.group(3) != kernel or m.group(4) != src:
+            continue
+        if m.group(2) is None:
+            return float(m.group(5))
+        if touched and scaled is None:
+            scaled = float(m.group(5)) * touched / int(m.group(6))
+    return round(scaled) if scaled is not None else None
 
 
 def assemble_line(**kw) -> str:
@@ -375,26 +402,73 @@ def cpu_baseline(d, wl, name: str, target_s: float, precision: str = "bf16", gx:
 
 # ------------------------------------------------------------------------------ our path
 
-def run_ours(args, rank, world, local_rank):
-    import torch
-
-    from mixture_experts_routed_topk_gb300 import binding, build
+def workload_for(args, name):
+    """The workload `name`, with the --tokens / --experts overrides applied to the primary one."""
     from mixture_experts_routed_topk_gb300 import workloads as W
 
-    build.build()
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    dist = dist_init(world, "nccl")
+    wl = W.WORKLOADS[name]
+    if name == args.config:
+        if args.tokens:
+            wl = dataclasses.replace(wl, T=int(args.tokens))
+        if args.experts:
+            wl = dataclasses.replace(wl, E=int(args.experts))
+    return wl
 
-    wl = W.WORKLOADS[args.config]
-    if args.tokens:
-        wl = dataclasses.replace(wl, T=int(args.tokens))
+
+def workload_label(args, name, wl):
+    base = __import__("mixture_experts_routed_topk_gb300.workloads", fromlist=["WORKLOADS"]).WORKLOADS[name]
+    changed = [f"{k}={getattr(wl, k)}" for k in ("T", "E") if getattr(wl, k) != getattr(base, k)]
+    return name if not changed else f"{name} ({', '.join(changed)})"
+
+
+class WeightCache:
+    """The expert weights of one (E, D, F) at a time, and their prepared block-scaled forms: the
+    decode and large workloads share their shapes, so they share one 22.5 GB weight set."""
+
+    def __init__(self, device, seed):
+        self.device, self.seed, self.key, self.w, self.prepared = device, seed, None, None, {}
+
+    def get(self, E, D, F):
+        from mixture_experts_routed_topk_gb300 import workloads as W
+        import torch
+
+        if self.key != (E, D, F):
+            self.w, self.prepared = None, {}
+            torch.cuda.empty_cache()
+            self.w = W.make_weights(E, D, F, self.seed, self.device)
+            self.key = (E, D, F)
+        return self.w
+
+    def prepare(self, precision):
+        """Block-scaled weights, prepared once per weight set (outside every timed region)."""
+        from mixture_experts_routed_topk_gb300 import binding
+
+        if precision not in self.prepared:
+            w13, w2 = self.w
+            if precision == "mxfp8":
+                self.prepared[precision] = (binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W13, w13),
+                                            binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W2, w2))
+            else:
+                self.prepared[precision] = (binding.moe_nvfp4_prepare_weight(binding.MOE_WEIGHT_W13, w13),
+                                            binding.moe_nvfp4_prepare_weight(binding.MOE_WEIGHT_W2, w2))
+        return self.prepared[precision]
+
+
+def measure_forward(args, name, device, dist, rank, world, cache, cpu_seconds):
+    """Times one workload's forward (the stage calls with events, then the whole call end to end on
+    host buffers) and returns its fields for the JSON line (rank 0; None on the other ranks)."""
+    import torch
+
+    from mixture_experts_routed_topk_gb300 import binding
+    from mixture_experts_routed_topk_gb300 import workloads as W
+
+    wl = workload_for(args, name)
     T, D, F, E, K = wl.dims()
     rseed = replica_seed(args.seed, rank)
     x = W.make_x(T, D, rseed, device)
     ids = W.make_topk_ids(T, E, K, wl.routing, rseed, device)
     scores = W.make_scores(T, K, wl.scores, rseed, device)
-    w13, w2 = W.make_weights(E, D, F, args.seed, device)
+    w13, w2 = cache.get(E, D, F)
     dims = (T, D, F, E, K)
     prec = PRECISIONS[args.precision]
     mx = args.precision == "mxfp8"
@@ -405,12 +479,10 @@ def run_ours(args, rank, world, local_rank):
     stages = MEGA_STAGES if mega else STAGES
     gx = 0.0
     if mx:  # prepared once, as the pages prepare block-scaled weights before execution
-        w13_mx = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W13, w13)
-        w2_mx = binding.moe_mxfp8_prepare_weight(binding.MOE_WEIGHT_W2, w2)
+        w13_mx, w2_mx = cache.prepare("mxfp8")
         ws = binding.alloc_workspace(binding.moe_mxfp8_workspace_bytes(*dims), device)
     elif nv:  # weights prepared once; x's tensor scale calibrated from this batch, h's a constant
-        w13_nv = binding.moe_nvfp4_prepare_weight(binding.MOE_WEIGHT_W13, w13)
-        w2_nv = binding.moe_nvfp4_prepare_weight(binding.MOE_WEIGHT_W2, w2)
+        w13_nv, w2_nv = cache.prepare("nvfp4")
         gx = float(torch.tensor(x.abs().max().float().item(), dtype=torch.float32) / 2688.0)
         ws = binding.alloc_workspace(binding.moe_nvfp4_workspace_bytes(*dims), device)
     elif mega:
@@ -463,7 +535,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(device)
     status = binding.moe_get_status(ws, stream)
     if status != 0:
-        raise RuntimeError(f"device status bits {status:#x} after warm-up")
+        raise RuntimeError(f"device status bits {status:#x} after warm-up ({name})")
     counts = (binding.moe_mxfp8_workspace_layout(*dims) if mx else
               binding.moe_nvfp4_workspace_layout(*dims) if nv else
               binding.moe_mega_workspace_layout(*dims) if mega else binding.moe_workspace_layout(*dims))
@@ -472,8 +544,8 @@ def run_ours(args, rank, world, local_rank):
 
     # ------------------------------------------------------------------ device-timed region
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
-    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid) if hasattr(
-        torch.cuda.get_device_properties(device), "uuid") else str(local_rank)
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(device.index)
     sampler = ClockSampler(gpu_id)
     sampler.start()
     barrier(dist, device)
@@ -561,11 +633,11 @@ def run_ours(args, rank, world, local_rank):
     e2e_s = reduce_max(dist, e2e_start.elapsed_time(e2e_end) / 1e3)
     h2d = x.numel() * 2 + ids.numel() * 4 + scores.numel() * 4
     d2h = out.numel() * 2
+    del x_d, out_d, ids_d, scores_d, flush
 
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
-        return
+        del ws, out
+        return None
 
     peaks, peak_src = measured_peaks()
     costs = kernel_costs(T, D, F, E, K, touched, None if args.precision == "bf16" else prec["elem_bytes"])
@@ -574,49 +646,94 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = total_s * 1e3 / args.steps
     sustained = ms_per_step * args.steps > 2000.0  # a seconds-long loop runs under the power cap
     tensor_scale = prec["tensor_scale"]
+    label = workload_label(args, name, wl)
     roof = roofline_entry(dominant, costs, mean_stage[dominant] / 1e3, peaks, sustained,
-                          recorded_traffic(args.config, prec["key"] + dominant), tensor_scale)
+                          recorded_traffic(name, prec["key"] + dominant, touched), tensor_scale)
     roof["peak_source"] = peak_src
     flops, alg_bytes = path_costs(T, D, F, E, K, touched, prec["elem_bytes"])
     step_s = ms_per_step / 1e3
     t_roof = max(flops / (tensor_scale * peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
+    path_bound = "tensor" if flops / (tensor_scale * peaks["bf16_tflops"] * 1e12) >= alg_bytes / (
+        peaks["hbm_gbs"] * 1e9) else "hbm"
+    stage_roofs = {s: roofline_entry(s, costs, mean_stage[s] / 1e3, peaks, sustained,
+                                     recorded_traffic(name, prec["key"] + s, touched), tensor_scale)
+                   for s in stages}
 
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline({"x": x, "topk_ids": ids, "topk_scores": scores, "w13": w13, "w2": w2}, wl,
-                           args.config, args.cpu_seconds, args.precision, gx)
+                           label, cpu_seconds, args.precision, gx)
+    del ws, out
+    return {
+        "value": round(world * T * args.steps / total_s, 1),
+        "ms_per_step": round(ms_per_step, 4),
+        "config": {"workload": label, "T": T, "D": D, "F": F, "E": E, "K": K,
+                   "precision": args.precision, "pipeline": args.pipeline, "routing": wl.routing,
+                   "experts_touched": touched, "global_batch": T * world, "parallelism": f"replicas{world}",
+                   "l2": "flushed between steps (512 MB write)", "seed": args.seed},
+        "tflops": round(world * flops / step_s / 1e12, 2),
+        "path_roofline": {"bound": path_bound, "ms": round(t_roof * 1e3, 4), "frac": round(t_roof / step_s, 4),
+                          "flops": flops, "alg_bytes": alg_bytes,
+                          "hbm_gbs": round(alg_bytes / step_s / 1e9, 1),
+                          "overhead_bytes": {k: int(v) for k, v in
+                                             overhead_bytes(T, D, F, K, prec["elem_bytes"]).items()}},
+        "roofline": roof,
+        "stage_ms": {s: round(v, 4) for s, v in mean_stage.items()},
+        "stage_roofline": {s: {k: r[k] for k in ("bound", "achieved", "unit", "frac", "traffic")}
+                           for s, r in stage_roofs.items()},
+        "e2e": {"value": round(world * T * args.steps / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": (MEGA_KERNELS_PER_STEP if mega else KERNELS_PER_STEP) * args.steps,
+        "clocks": sampler.summary(),
+        "wall_s": round(wall, 3),
+        "cpu_baseline": cpu,
+    }
 
-    line = assemble_line(
-        metric=METRIC,
-        value=round(world * T * args.steps / total_s, 1),
-        unit="tokens/s",
-        n_gpus=world,
-        steps=args.steps,
-        warmup=args.warmup,
-        ms_per_step=round(ms_per_step, 4),
-        higher_is_better=True,
-        scaling="weak",
-        vs_baseline=None,
-        dtype=prec["dtype"],
-        data="synthetic",
-        config={"workload": args.config if not args.tokens else f"{args.config} (T={T})", "T": T, "D": D, "F": F,
-                "precision": args.precision, "pipeline": args.pipeline,
-                "E": E, "K": K, "routing": wl.routing, "experts_touched": touched, "global_batch": T * world, "parallelism": f"replicas{world}",
-                "l2": "flushed between steps (512 MB write)", "seed": args.seed},
-        tflops=round(world * flops / step_s / 1e12, 2),
-        path_roofline={"ms": round(t_roof * 1e3, 4), "frac": round(t_roof / step_s, 4),
-                       "flops": flops, "alg_bytes": alg_bytes,
-                       "overhead_bytes": {k: int(v) for k, v in overhead_bytes(T, D, F, K, prec["elem_bytes"]).items()}},
-        roofline=roof,
-        stage_ms={s: round(v, 4) for s, v in mean_stage.items()},
-        e2e={"value": round(world * T * args.steps / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-             "d2h_bytes_per_step": d2h},
-        gpu_launches=(MEGA_KERNELS_PER_STEP if mega else KERNELS_PER_STEP) * args.steps,
-        clocks=sampler.summary(),
-        wall_s=round(wall, 3),
-        cpu_baseline=cpu,
-    )
-    print(line, flush=True)
+
+def extra_workloads(args) -> list[str]:
+    """The workloads measured after the primary one and reported as sub-records of its line."""
+    if args.tokens or args.experts or not args.also:
+        return []
+    names = [n.strip() for n in args.also.split(",") if n.strip()]
+    return [n for n in names if n != args.config]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from mixture_experts_routed_topk_gb300 import binding, build
+
+    build.build()
+    binding.load()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+    cache = WeightCache(device, args.seed)
+    prec = PRECISIONS[args.precision]
+
+    main = measure_forward(args, args.config, device, dist, rank, world, cache, args.cpu_seconds)
+    subs = {}
+    for name in extra_workloads(args):
+        subs[name] = measure_forward(args, name, device, dist, rank, world, cache, args.sub_cpu_seconds)
+    if rank == 0:
+        fields = dict(
+            metric=METRIC,
+            value=main["value"],
+            unit="tokens/s",
+            n_gpus=world,
+            steps=args.steps,
+            warmup=args.warmup,
+            ms_per_step=main["ms_per_step"],
+            higher_is_better=True,
+            scaling="weak",
+            vs_baseline=None,
+            dtype=prec["dtype"],
+            data="synthetic",
+        )
+        fields.update({k: v for k, v in main.items() if k not in ("value", "ms_per_step")})
+        for name, rec in subs.items():
+            fields[name] = rec
+        print(assemble_line(**fields), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 

@@ -501,12 +501,13 @@ moe_status_t moe_fwd_nvfp4_stages(const void *x, const int32_t *topk_ids, const 
  * loads the library until the process exits. Sizes with (E + 1) * ceil(T*K / 2048) above
  * MOE_STATIC_SCRATCH_MAX_ENTRIES return MOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
  *
- * Set-up: the first call on a device (with that device current) looks up the array's device
- * address with cudaGetSymbolAddress and caches it; make that first call before any stream
- * capture. Every call on a device shares the one array and it keeps the previous call's
- * contents; the call rewrites all of the scratch it reads. Calls whose GPU work overlaps (on
- * different streams, or from different threads without ordering) race on the array: order them
- * on one stream.
+ * Set-up: every call looks up the array's device address on the current device with
+ * cudaGetSymbolAddress (nothing is cached, so a device reset, after which the array may move, needs
+ * no special handling). The first lookup on a device may load the library's device code: make the
+ * first call on each device before any stream capture. Every call on a device shares the one array
+ * and it keeps the previous call's contents; the call clears the status slot it uses and rewrites
+ * all of the other scratch it reads. Calls whose GPU work overlaps (on different streams, or from
+ * different threads without ordering) race on the array: order them on one stream.
  */
 moe_status_t moe_routing_static_scratch(const int32_t *topk_ids, int64_t T, int32_t E, int32_t K,
                                         int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv,

@@ -148,6 +148,25 @@ def _need(t: torch.Tensor, name: str, dtype=None, ndim=None, cuda=True):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _need_routing_outputs(counts, offsets, perm, inv, T: int, E: int, K: int):
+    """int32 CUDA outputs of the routing calls, large enough for what the kernels write: counts [E],
+    offsets [E+1], perm and inv [T*K]."""
+    for name, t, n in (("counts", counts, E), ("offsets", offsets, E + 1), ("perm", perm, T * K),
+                       ("inv", inv, T * K)):
+        _need(t, name, torch.int32)
+        if t.numel() < n:
+            raise ValueError(f"{name} must hold at least {n} int32, got {t.numel()}")
+
+
+def _need_status_word(t):
+    """A caller-owned device status word: the library clears and ORs one whole uint32."""
+    _need(t, "device_status", (torch.int32, torch.uint8))
+    if t.numel() * t.element_size() < 4:
+        raise ValueError(f"device_status must hold at least 4 bytes, got {t.numel() * t.element_size()}")
+    if t.data_ptr() % 4:
+        raise ValueError("device_status must be 4-byte aligned")
+
+
 def _dims(x, topk_ids, w13):
     T, D = x.shape
     E, two, F, D2 = w13.shape
@@ -194,10 +213,9 @@ def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
 
 def moe_routing(topk_ids, num_experts: int, counts, offsets, perm, inv, workspace, stream=None) -> None:
     _need(topk_ids, "topk_ids", torch.int32, 2)
-    for name, t in (("counts", counts), ("offsets", offsets), ("perm", perm), ("inv", inv)):
-        _need(t, name, torch.int32)
-    _need(workspace, "workspace", torch.uint8)
     T, K = topk_ids.shape
+    _need_routing_outputs(counts, offsets, perm, inv, T, int(num_experts), K)
+    _need(workspace, "workspace", torch.uint8)
     _check("moe_routing", load().moe_routing(
         _ptr(topk_ids), T, int(num_experts), K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
         _ptr(workspace), workspace.numel(), _stream_handle(stream)))
@@ -323,11 +341,10 @@ def moe_routing_static_scratch(topk_ids, num_experts: int, counts, offsets, perm
     Calls share the array, so calls whose GPU work overlaps race: order them on one stream.
     """
     _need(topk_ids, "topk_ids", torch.int32, 2)
-    for name, t in (("counts", counts), ("offsets", offsets), ("perm", perm), ("inv", inv)):
-        _need(t, name, torch.int32)
-    if device_status is not None:
-        _need(device_status, "device_status", (torch.int32, torch.uint8))
     T, K = topk_ids.shape
+    _need_routing_outputs(counts, offsets, perm, inv, T, int(num_experts), K)
+    if device_status is not None:
+        _need_status_word(device_status)
     _check("moe_routing_static_scratch", load().moe_routing_static_scratch(
         _ptr(topk_ids), T, int(num_experts), K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
         _ptr(device_status), _stream_handle(stream)))
@@ -365,7 +382,7 @@ def moe_routed_experts_bwd(x, topk_ids, topk_scores, w13, w2, dout, dx, dscores,
 
 def moe_selftest_wait_timeout(timeout_us: int, device_status, stream=None) -> None:
     """Runs a kernel whose bounded wait must run out; device_status receives MOE_DEV_TIMEOUT."""
-    _need(device_status, "device_status", (torch.int32, torch.uint8))
+    _need_status_word(device_status)
     _check("moe_selftest_wait_timeout", load().moe_selftest_wait_timeout(
         int(timeout_us), _ptr(device_status), _stream_handle(stream)))
 

@@ -3,12 +3,12 @@
 // callers that cannot allocate a routing workspace.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the library holds it until
-// the process exits. Host code cannot use the array's name as a device address, so the first call
-// on each device looks the address up with cudaGetSymbolAddress (with that device current) and
-// caches it; later calls on that device reuse it.
+// the process exits. Host code cannot use the array's name as a device address, so every call looks
+// the address up with cudaGetSymbolAddress on the current device. Nothing is cached: after a device
+// reset the library's device code is loaded again and the array may sit at another address. The
+// first lookup on a device may load the library's device code, which is why a caller makes its
+// first call on a device before any stream capture; later lookups are plain host queries.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -22,20 +22,11 @@ namespace {
 constexpr int64_t kStaticEntries = MOE_STATIC_SCRATCH_MAX_ENTRIES;
 constexpr int64_t kStatusSlotInts = 64;  // 256 bytes: a status word for callers that pass none
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-int32_t* g_scratch_address[kMaxDevices];  // per device; null until that device's first call
-
+// The array's device address on the current device, looked up afresh by every call.
 moe_status_t scratch_address(int32_t** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_address[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_routing_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-        g_scratch_address[dev] = static_cast<int32_t*>(p);
-    }
-    *out = g_scratch_address[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_routing_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    *out = static_cast<int32_t*>(p);
     return MOE_OK;
 }
 

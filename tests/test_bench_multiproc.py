@@ -54,7 +54,9 @@ def test_single_process_defaults(monkeypatch):
     assert bench.dist_init(1, "gloo") is None
     assert bench.reduce_max(None, 3.5) == 3.5
     args = bench.parse_args([])
-    assert args.gpus == 1 and args.config == "medium" and args.impl == "ours" and args.warmup >= 3
+    assert args.gpus == 1 and args.config == "large" and args.impl == "ours" and args.warmup >= 3
+    assert bench.extra_workloads(args) == ["decode", "medium"]
+    assert bench.extra_workloads(bench.parse_args(["--experts", "16", "--config", "decode"])) == []
 
 
 def test_roofline_arithmetic():

@@ -69,3 +69,24 @@ def test_routing_empty_is_noop():
     z = torch.empty(0, dtype=torch.int32, device="cuda")
     binding.moe_routing(ids, 8, torch.empty(8, dtype=torch.int32, device="cuda"),
                         torch.empty(9, dtype=torch.int32, device="cuda"), z, z, ws)
+
+
+@pytest.mark.parametrize("short", ["counts", "offsets", "perm", "inv"])
+def test_binding_rejects_short_routing_outputs(short):
+    # outputs too small for what the kernels write are refused before anything is enqueued
+    T, E, K = 100, 16, 4
+    ids = torch.zeros((T, K), dtype=torch.int32, device="cuda")
+    sizes = {"counts": E, "offsets": E + 1, "perm": T * K, "inv": T * K}
+    sizes[short] -= 1
+    outs = [torch.zeros(sizes[n], dtype=torch.int32, device="cuda") for n in ("counts", "offsets", "perm", "inv")]
+    ws = binding.alloc_workspace(binding.moe_routing_workspace_bytes(T, E, K), "cuda")
+    with pytest.raises(ValueError, match=short):
+        binding.moe_routing(ids, E, *outs, ws)
+    with pytest.raises(ValueError, match=short):
+        binding.moe_routing_static_scratch(ids, E, *outs)
+
+
+def test_binding_rejects_short_status_word():
+    status = torch.zeros(3, dtype=torch.uint8, device="cuda")  # the library writes a whole uint32
+    with pytest.raises(ValueError, match="device_status"):
+        binding.moe_selftest_wait_timeout(10, status)

@@ -155,15 +155,17 @@ def kernel_costs(T, D, F, E, K, touched, q=None):
     """Algorithmic flops and bytes per launch of each stage (tile padding not counted). q: bytes per
     element of the block-scaled operands (codes + scales), None for the bf16 forward."""
     R = T * K
+    # dispatch: ids read twice (histogram, permute), perm and inv written, then the token-order
+    # gather: each x row read once and written to its K routed rows
     if q is not None:
         return {
-            "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + R * D * 2 + R * D * q},
+            "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + T * D * 2 + R * D * q},
             "gemm1_swiglu": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * q + R * D * q + R * F * q},
             "gemm2_score": {"flops": 2 * R * D * F, "bytes": touched * D * F * q + R * F * q + R * D * 2 + R * 8},
             "combine": {"flops": 0, "bytes": R * D * 2 + T * D * 2 + R * 4},
         }
     return {
-        "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + 2 * R * D * 2},
+        "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + T * D * 2 + R * D * 2},
         "gemm1_swiglu": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * 2 + R * D * 2 + R * F * 2},
         "gemm2_score": {"flops": 2 * R * D * F, "bytes": touched * D * F * 2 + R * F * 2 + R * D * 2 + R * 8},
         # both GEMMs in one grid: H stays inside the kernel, so only XP in and Y out count

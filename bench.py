@@ -56,6 +56,8 @@ STAGES = ("dispatch", "gemm1_swiglu", "gemm2_score", "combine")
 KERNELS_PER_STEP = 7  # hist, scan, permute, gather, gemm1, gemm2, combine
 MEGA_STAGES = ("dispatch", "fused_gemms", "combine")
 MEGA_KERNELS_PER_STEP = 6  # hist, scan, permute, gather, the fused GEMMs, combine
+# backward: hist, scan, permute, pad tiles, pad rows, gather; recompute, two dgrads, two wgrads; dscores, dx
+BWD_KERNELS_PER_STEP = 13
 
 # Operand formats of the forward: bytes per quantized element (codes + scales), the tensor peak as
 # a multiple of the measured bf16 peak (nominal dense ratios: fp8 4.5 / 2.25, fp4 13.5 / 2.25), the
@@ -742,8 +744,54 @@ def run_ours(args, rank, world, local_rank):
 
 # ------------------------------------------------------------------------------ backward pass
 
+def bwd_stage_costs(T, D, F, E, K, touched):
+    """Algorithmic flops and bytes of each backward stage (padding rows not counted): touched
+    experts' weights, the routed rows each stage reads and writes, the weight gradients."""
+    R = T * K
+    ntf = -(-F // 256)  # dscores partial sums per pair (one per 256-column tile of the F axis)
+    return {
+        "dispatch": {"flops": 0, "bytes": 2 * R * 4 + 2 * R * 4 + 2 * T * D * 2 + 2 * R * D * 2},
+        "recompute": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * 2 + R * D * 2 + R * 3 * F * 2},
+        "dgrad_down": {"flops": 2 * R * D * F,
+                       "bytes": touched * D * F * 2 + R * D * 2 + R * 2 * F * 2 + R * 2 * F * 2 + R * ntf * 4},
+        "dgrad_gate_up": {"flops": 4 * R * D * F, "bytes": touched * 2 * F * D * 2 + R * 2 * F * 2 + R * D * 2},
+        "wgrad_down": {"flops": 2 * R * D * F, "bytes": R * D * 2 + R * F * 2 + E * D * F * 2},
+        "wgrad_gate_up": {"flops": 4 * R * D * F, "bytes": R * 2 * F * 2 + R * D * 2 + E * 2 * F * D * 2},
+        "reduce": {"flops": 0, "bytes": R * D * 2 + R * ntf * 4 + T * D * 2 + T * K * 4},
+    }
+
+
+def cpu_baseline_bwd(d, wl, name: str, target_s: float) -> dict:
+    """The oracle's backward on the host cores: a bounded token sample, repeated to fill about
+    target_s seconds (tokens/s = tokens processed / seconds)."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    ids_host = d["topk_ids"].cpu().numpy()
+    # the backward does about 16/6 of the forward's work per token (recompute, two dgrads, two wgrads)
+    n_tok = bounded_tokens(ids_host, wl, max(1, oracle_tokens_for(target_s, wl, cores) * 6 // 16))
+    sample = oracle_sample(d, n_tok)
+    dout = d["dout"][:n_tok].float().cpu().numpy()
+
+    def once():
+        t0 = time.perf_counter()
+        oracle.routed_experts_bwd(sample["x"], sample["ids"], sample["scores"], sample["w13"], sample["w2"], dout,
+                                  nthreads=cores)
+        return time.perf_counter() - t0
+
+    secs = [once()]
+    reps = max(1, min(100, int(target_s / max(secs[0], 1e-6))))
+    secs += [once() for _ in range(reps - 1)]
+    total = sum(secs)
+    return {"value": round(n_tok * len(secs) / total, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"backward of the first {n_tok} tokens of the {name} workload ({sample['experts']} experts "
+                      f"touched, full K={wl.K} per token) x {len(secs)} runs = {total:.1f} s on {cores} threads",
+            "seconds": round(total, 2)}
+
+
 def run_ours_bwd(args, rank, world, local_rank):
-    """Times moe_routed_experts_bwd: dx, dscores, dw13, dw2 for one upstream gradient per step."""
+    """Times the backward as its seven stage calls (moe_bwd_stages), with events between them: dx,
+    dscores, dw13, dw2 for one upstream gradient per step."""
     import torch
 
     from mixture_experts_routed_topk_gb300 import binding, build
@@ -753,9 +801,7 @@ def run_ours_bwd(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     dist = dist_init(world, "nccl")
-    wl = W.WORKLOADS[args.config]
-    if args.tokens:
-        wl = dataclasses.replace(wl, T=int(args.tokens))
+    wl = workload_for(args, args.config)
     T, D, F, E, K = wl.dims()
     rseed = replica_seed(args.seed, rank)
     x = W.make_x(T, D, rseed, device)
@@ -769,9 +815,15 @@ def run_ours_bwd(args, rank, world, local_rank):
     dw13, dw2 = torch.empty_like(w13), torch.empty_like(w2)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
+    stages = binding.BWD_STAGE_NAMES
 
-    def step():
-        binding.moe_routed_experts_bwd(x, ids, scores, w13, w2, dout, dx, dscores, dw13, dw2, ws, stream)
+    def step(ev=None):
+        for s in range(binding.BWD_STAGES):
+            if ev is not None:
+                ev[s].record(stream)
+            binding.moe_bwd_stages(x, ids, scores, w13, w2, dout, dx, dscores, dw13, dw2, ws, s, s + 1, stream)
+        if ev is not None:
+            ev[binding.BWD_STAGES].record(stream)
 
     for _ in range(max(args.warmup, 0)):
         flush.zero_()
@@ -779,20 +831,43 @@ def run_ours_bwd(args, rank, world, local_rank):
     torch.cuda.synchronize(device)
     if binding.moe_get_status(ws, stream) != 0:
         raise RuntimeError("device status bits after warm-up")
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    touched = int((torch.bincount(ids[(ids >= 0) & (ids < E)].long(), minlength=E) > 0).sum().item())
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(device).uuid))
     sampler.start()
     barrier(dist, device)
     torch.cuda.synchronize(device)
     for i in range(args.steps):
         flush.zero_()
-        events[i][0].record(stream)
-        step()
-        events[i][1].record(stream)
+        step(events[i])
     torch.cuda.synchronize(device)
     barrier(dist, device)
     sampler.stop()
-    total_s = reduce_max(dist, sum(e[0].elapsed_time(e[1]) for e in events) / 1e3)
+    stage_ms = {s: statistics.mean(events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps))
+                for j, s in enumerate(stages)}
+    total_s = reduce_max(dist, sum(e[0].elapsed_time(e[len(stages)]) for e in events) / 1e3)
+
+    # end to end: each step uploads x, ids, scores and dout from pinned host memory and reads dx and
+    # dscores back, inside the timed region (the weight gradients stay on the device for the optimizer)
+    x_h, ids_h, sc_h, go_h = (t.cpu().pin_memory() for t in (x, ids, scores, dout))
+    dx_h = torch.empty((T, D), dtype=torch.bfloat16).pin_memory()
+    ds_h = torch.empty((T, K), dtype=torch.float32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_h, non_blocking=True)
+        ids.copy_(ids_h, non_blocking=True)
+        scores.copy_(sc_h, non_blocking=True)
+        dout.copy_(go_h, non_blocking=True)
+        binding.moe_routed_experts_bwd(x, ids, scores, w13, w2, dout, dx, dscores, dw13, dw2, ws, stream)
+        dx_h.copy_(dx, non_blocking=True)
+        ds_h.copy_(dscores, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    e2e_s = reduce_max(dist, e0.elapsed_time(e1) / 1e3)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -805,18 +880,41 @@ def run_ours_bwd(args, rank, world, local_rank):
     achieved = world * flops / step_s / 1e12
     sustained = total_s > 2.0
     peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    costs = bwd_stage_costs(T, D, F, E, K, touched)
+    label = workload_label(args, args.config, wl)
+    stage_roofs = {s: roofline_entry(s, costs, stage_ms[s] / 1e3, peaks, sustained,
+                                     recorded_traffic(args.config, "bwd_" + s, touched))
+                   for s in stages}
+    gemms = [s for s in stages if costs[s]["flops"] > 0]
+    dominant = max(gemms, key=lambda s: stage_ms[s])
+    furthest = min(gemms, key=lambda s: stage_roofs[s]["frac"])
+    roof = dict(stage_roofs[dominant])
+    roof["peak_source"] = peak_src
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline_bwd({"x": x, "topk_ids": ids, "topk_scores": scores, "w13": w13, "w2": w2,
+                                "dout": dout}, wl, label, args.cpu_seconds)
     print(assemble_line(
         metric="routed-expert bwd tokens/s and TFLOP/s on 1 GB300; % of roofline",
         value=round(world * T * args.steps / total_s, 1), unit="tokens/s", n_gpus=world, steps=args.steps,
         warmup=args.warmup, ms_per_step=round(step_s * 1e3, 4), higher_is_better=True, scaling="weak",
         vs_baseline=None, dtype="bf16", data="synthetic",
-        config={"workload": args.config if not args.tokens else f"{args.config} (T={T})", "T": T, "D": D, "F": F,
-                "E": E, "K": K, "routing": wl.routing, "pass": "bwd", "l2": "flushed between steps (512 MB write)"},
+        config={"workload": label, "T": T, "D": D, "F": F, "E": E, "K": K, "routing": wl.routing,
+                "experts_touched": touched, "pass": "bwd", "l2": "flushed between steps (512 MB write)"},
         tflops=round(achieved, 2),
-        roofline={"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                  "frac": round(achieved / peak, 4), "traffic": None, "kernel": "whole backward call (16 RDF flops)",
-                  "peak_kind": "sustained" if sustained else "burst", "peak_source": peak_src},
-        gpu_launches=None, clocks=sampler.summary(), cpu_baseline=None,
+        path_roofline={"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                       "frac": round(achieved / peak, 4), "flops": flops,
+                       "peak_kind": "sustained" if sustained else "burst"},
+        roofline=roof,
+        stage_ms={s: round(v, 4) for s, v in stage_ms.items()},
+        stage_roofline={s: {k: r[k] for k in ("bound", "achieved", "unit", "frac", "traffic")}
+                        for s, r in stage_roofs.items()},
+        furthest_below_roof={"stage": furthest, "frac": stage_roofs[furthest]["frac"],
+                             "achieved": stage_roofs[furthest]["achieved"], "unit": stage_roofs[furthest]["unit"]},
+        e2e={"value": round(world * T * args.steps / e2e_s, 1), "unit": "tokens/s",
+             "h2d_bytes_per_step": x.numel() * 2 + ids.numel() * 4 + scores.numel() * 4 + dout.numel() * 2,
+             "d2h_bytes_per_step": dx.numel() * 2 + dscores.numel() * 4},
+        gpu_launches=BWD_KERNELS_PER_STEP * args.steps, clocks=sampler.summary(), cpu_baseline=cpu,
     ), flush=True)
     if dist is not None:
         dist.destroy_process_group()

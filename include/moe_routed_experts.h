@@ -289,6 +289,33 @@ moe_status_t moe_routed_experts_bwd(const void *x, const int32_t *topk_ids, cons
                                     int32_t F, int32_t E, int32_t K, void *workspace, size_t workspace_bytes,
                                     moe_stream_t stream);
 
+/* Stages of the backward pass, for moe_bwd_stages. */
+enum {
+    MOE_BWD_STAGE_DISPATCH = 0,      /* status cleared, routing, padded-row maps, x and dout rows gathered */
+    MOE_BWD_STAGE_RECOMPUTE = 1,     /* gate/up GEMM again: GU = [g | u] and HS = s h per padded row      */
+    MOE_BWD_STAGE_DGRAD_DOWN = 2,    /* dout rows x W2 with the SwiGLU backward: DGU = [dg | du], dscores  */
+                                     /* partial sums                                                        */
+    MOE_BWD_STAGE_DGRAD_GATE_UP = 3, /* DGU x w13: the pairs' dx rows                                      */
+    MOE_BWD_STAGE_WGRAD_DOWN = 4,    /* dw2[e] = (s dout)^T h over the expert's rows                         */
+    MOE_BWD_STAGE_WGRAD_GATE_UP = 5, /* dw13[e] = [dg; du]^T x over the expert's rows                        */
+    MOE_BWD_STAGE_REDUCE = 6,        /* dscores and dx, each summed in a fixed order                        */
+    MOE_BWD_STAGES = 7
+};
+
+/*
+ * Stages stage_begin .. stage_end-1 (MOE_BWD_STAGE_*) of moe_routed_experts_bwd, on one workspace:
+ * a stage reads what the earlier stages left in it, so a caller runs the stages in order (one call
+ * per stage lets it time each with events on its stream). 0 <= stage_begin <= stage_end <=
+ * MOE_BWD_STAGES; the full range is moe_routed_experts_bwd. Arguments and errors as for that call;
+ * MOE_ERR_INVALID_ARG for a bad range. With T = 0 the weight-gradient stages write zeros and the
+ * others do nothing.
+ */
+moe_status_t moe_bwd_stages(const void *x, const int32_t *topk_ids, const void *topk_scores,
+                            int32_t scores_dtype, const void *w13, const void *w2, const void *dout,
+                            void *dx, float *dscores, void *dw13, void *dw2, int64_t T, int32_t D,
+                            int32_t F, int32_t E, int32_t K, int32_t stage_begin, int32_t stage_end,
+                            void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------ */
 /* MXFP8 forward (Dist-MoE 0.1.0, "Choose a precision and pipeline / MXFP8": MXFP8 E4M3, the    */
 /* activations quantized after routing, the weights prepared once and reused -- "Use advanced   */

@@ -86,6 +86,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "moe_bwd_workspace_bytes": ([i64, i32, i32, i32, i32], sz),
             "moe_routed_experts_bwd": (
                 [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, sz, vp], ctypes.c_int),
+            "moe_bwd_stages": (
+                [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, vp, sz, vp],
+                ctypes.c_int),
             "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "moe_mxfp8_weight_bytes": ([i32, i32, i32, i32, vp, vp], ctypes.c_int),
             "moe_mxfp8_prepare_weight": ([i32, vp, i32, i32, i32, vp, sz, vp, sz, vp], ctypes.c_int),
@@ -354,9 +357,28 @@ def moe_bwd_workspace_bytes(T: int, D: int, F: int, E: int, K: int) -> int:
     return int(load().moe_bwd_workspace_bytes(T, D, F, E, K))
 
 
+BWD_STAGES = 7  # dispatch, recompute, dgrad down, dgrad gate/up, wgrad down, wgrad gate/up, reduce
+BWD_STAGE_NAMES = ("dispatch", "recompute", "dgrad_down", "dgrad_gate_up", "wgrad_down", "wgrad_gate_up", "reduce")
+
+
 def moe_routed_experts_bwd(x, topk_ids, topk_scores, w13, w2, dout, dx, dscores, dw13, dw2, workspace,
                            stream=None) -> None:
     """Gradients of the layer: dx [T,D] bf16, dscores [T,K] fp32, dw13 [E,2,F,D] and dw2 [E,D,F] bf16."""
+    args, dims = _bwd_args(x, topk_ids, topk_scores, w13, w2, dout, dx, dscores, dw13, dw2, workspace)
+    _check("moe_routed_experts_bwd", load().moe_routed_experts_bwd(
+        *args, *dims, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def moe_bwd_stages(x, topk_ids, topk_scores, w13, w2, dout, dx, dscores, dw13, dw2, workspace, stage_begin: int,
+                   stage_end: int, stream=None) -> None:
+    """Backward stages stage_begin .. stage_end-1 (BWD_STAGE_NAMES) on one workspace, in order."""
+    args, dims = _bwd_args(x, topk_ids, topk_scores, w13, w2, dout, dx, dscores, dw13, dw2, workspace)
+    _check("moe_bwd_stages", load().moe_bwd_stages(
+        *args, *dims, int(stage_begin), int(stage_end), _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+
+
+def _bwd_args(x, topk_ids, topk_scores, w13, w2, dout, dx, dscores, dw13, dw2, workspace):
+    """Checked pointer arguments and (T, D, F, E, K) of the backward entry points."""
     _need(x, "x", torch.bfloat16, 2)
     _need(topk_ids, "topk_ids", torch.int32, 2)
     _need(topk_scores, "topk_scores", (torch.float32, torch.bfloat16), 2)
@@ -375,9 +397,8 @@ def moe_routed_experts_bwd(x, topk_ids, topk_scores, w13, w2, dout, dx, dscores,
         if tuple(t.shape) != shape:
             raise ValueError(f"{name} must be {shape}, got {tuple(t.shape)}")
     sd = MOE_SCORES_BF16 if topk_scores.dtype == torch.bfloat16 else MOE_SCORES_F32
-    _check("moe_routed_experts_bwd", load().moe_routed_experts_bwd(
-        _ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(dout), _ptr(dx), _ptr(dscores),
-        _ptr(dw13), _ptr(dw2), T, D, F, E, K, _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+    return ((_ptr(x), _ptr(topk_ids), _ptr(topk_scores), sd, _ptr(w13), _ptr(w2), _ptr(dout), _ptr(dx),
+             _ptr(dscores), _ptr(dw13), _ptr(dw2)), (T, D, F, E, K))
 
 
 def moe_selftest_wait_timeout(timeout_us: int, device_status, stream=None) -> None:

@@ -471,7 +471,8 @@ int grid_for(int64_t work, int per_block, int sm_count) {
 
 }  // namespace
 
-moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
+moe_status_t launch_backward(const BwdProblem& p, int stage_begin, int stage_end, cudaStream_t stream) {
+    auto run = [&](int stage) { return stage_begin <= stage && stage < stage_end; };
     const int64_t R = p.T * p.K;
     const int64_t rp = p.padded_rows;  // capacity of the padded buffers
     const int32_t D = p.D, F = p.F, E = p.E;
@@ -487,11 +488,12 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
     b.perm = p.perm;
     b.inv = p.inv;
     b.status = p.status;
+    moe_status_t st = MOE_OK;
+    if (run(MOE_BWD_STAGE_DISPATCH)) {
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream) != cudaSuccess ||
         cudaMemsetAsync(p.pperm, 0xff, sizeof(int32_t) * rp, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
-    moe_status_t st = launch_routing(b, stream);
-    if (st != MOE_OK) return st;
+    if ((st = launch_routing(b, stream)) != MOE_OK) return st;
     if (launch_pdl(k_pad_tiles, dim3(1), dim3(1024), 0, stream, static_cast<const int32_t*>(p.counts), E, p.pmt) !=
             cudaSuccess ||
         launch_pdl(k_pad_rows, dim3(grid_for(R, 256, p.sm_count)), dim3(256), 0, stream, p.ids,
@@ -503,6 +505,7 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
                    static_cast<const int32_t*>(p.pmt), E, p.K, p.T, D / 8, static_cast<uint4*>(p.xpp),
                    static_cast<uint4*>(p.dop)) != cudaSuccess)
         return MOE_ERR_CUDA;
+    }
 
     GemmArgs a{};
     a.pmt = p.pmt;
@@ -517,6 +520,7 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
     CUtensorMap ta, tb;
 
     // recompute: GU = [g | u], HS = s h
+    if (run(MOE_BWD_STAGE_RECOMPUTE)) {
     if (!make_tmap(&ta, p.xpp, D, rp, kBK, kBM) || !make_tmap(&tb, p.w13, D, static_cast<uint64_t>(E) * 2 * F, kBK, kBN1))
         return MOE_ERR_CUDA;
     a.kblocks = D / kBK;
@@ -525,8 +529,10 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
     if ((st = launch_gemm<BwdRecompute>(ta, tb, a, sm_count_grid(max_row_tiles * ceil_div(F, kBN1), p.sm_count),
                                         stream)) != MOE_OK)
         return st;
+    }
 
     // dgrad of the down projection + SwiGLU backward
+    if (run(MOE_BWD_STAGE_DGRAD_DOWN)) {
     if (!make_tmap(&ta, p.dop, D, rp, kBK, kBM) || !make_tmap(&tb, p.w2, F, static_cast<uint64_t>(E) * D, 64, kBK))
         return MOE_ERR_CUDA;
     a.kblocks = D / kBK;
@@ -536,8 +542,10 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
     if ((st = launch_gemm<BwdDgradDown>(ta, tb, a, sm_count_grid(max_row_tiles * ceil_div(F, kBN2), p.sm_count),
                                         stream)) != MOE_OK)
         return st;
+    }
 
     // dgrad of gate/up
+    if (run(MOE_BWD_STAGE_DGRAD_GATE_UP)) {
     if (!make_tmap(&ta, p.dgu, 2ull * F, rp, kBK, kBM) ||
         !make_tmap(&tb, p.w13, D, static_cast<uint64_t>(E) * 2 * F, 64, kBK))
         return MOE_ERR_CUDA;
@@ -546,8 +554,10 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
     if ((st = launch_gemm<BwdDgradGateUp>(ta, tb, a, sm_count_grid(max_row_tiles * ceil_div(D, kBN2), p.sm_count),
                                           stream)) != MOE_OK)
         return st;
+    }
 
     // wgrad of W2: dW2[e] [D, F] = DOP_e^T HS_e
+    if (run(MOE_BWD_STAGE_WGRAD_DOWN)) {
     if (!make_tmap(&ta, p.dop, D, rp, 64, kBK) || !make_tmap(&tb, p.hs, F, rp, 64, kBK)) return MOE_ERR_CUDA;
     a.mdim = D;
     a.ndim = F;
@@ -558,8 +568,10 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
                                     sm_count_grid(static_cast<int64_t>(E) * a.mtiles * a.ntiles, p.sm_count),
                                     stream)) != MOE_OK)
         return st;
+    }
 
     // wgrad of w13: dW13[e] [2F, D] = DGU_e^T XPP_e
+    if (run(MOE_BWD_STAGE_WGRAD_GATE_UP)) {
     if (!make_tmap(&ta, p.dgu, 2ull * F, rp, 64, kBK) || !make_tmap(&tb, p.xpp, D, rp, 64, kBK)) return MOE_ERR_CUDA;
     a.mdim = 2 * F;
     a.ndim = D;
@@ -570,8 +582,9 @@ moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream) {
                                     sm_count_grid(static_cast<int64_t>(E) * a.mtiles * a.ntiles, p.sm_count),
                                     stream)) != MOE_OK)
         return st;
+    }
 
-    if (launch_pdl(k_dscores, dim3(grid_for(R, 256, p.sm_count)), dim3(256), 0, stream,
+    if (run(MOE_BWD_STAGE_REDUCE) && launch_pdl(k_dscores, dim3(grid_for(R, 256, p.sm_count)), dim3(256), 0, stream,
                    static_cast<const int32_t*>(p.pinv), static_cast<const float*>(p.partial), R,
                    static_cast<int32_t>(ceil_div(F, kBN2)), p.dscores) != cudaSuccess ||
         launch_pdl(k_dx_combine, dim3(grid_for(p.T * (D / 8), 256, p.sm_count)), dim3(256), 0, stream,

@@ -536,22 +536,25 @@ size_t moe_bwd_workspace_bytes(int64_t T, int32_t D, int32_t F, int32_t E, int32
     return L.off[BW_TOTAL];
 }
 
-moe_status_t moe_routed_experts_bwd(const void* x, const int32_t* topk_ids, const void* topk_scores,
-                                    int32_t scores_dtype, const void* w13, const void* w2, const void* dout, void* dx,
-                                    float* dscores, void* dw13, void* dw2, int64_t T, int32_t D, int32_t F, int32_t E,
-                                    int32_t K, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+moe_status_t moe_bwd_stages(const void* x, const int32_t* topk_ids, const void* topk_scores, int32_t scores_dtype,
+                            const void* w13, const void* w2, const void* dout, void* dx, float* dscores, void* dw13,
+                            void* dw2, int64_t T, int32_t D, int32_t F, int32_t E, int32_t K, int32_t stage_begin,
+                            int32_t stage_end, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
     if (bad_scores_dtype(scores_dtype)) return MOE_ERR_INVALID_ARG;
+    if (stage_begin < 0 || stage_end > MOE_BWD_STAGES || stage_begin > stage_end) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(T, D, F, E, K, true);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK || stage_begin == stage_end) return st;
     if (!w13 || !w2 || !dw13 || !dw2) return MOE_ERR_INVALID_ARG;
     if (!aligned(w13, 16) || !aligned(w2, 16) || !aligned(dw13, 16) || !aligned(dw2, 16)) return MOE_ERR_MISALIGNED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DeviceInfo dev;
     if (T == 0) {
-        // no tokens: the weight gradients are zero
+        // no tokens: the weight gradients are zero (written by the stages that write them)
         if ((st = device_info(&dev)) != MOE_OK) return st;
-        if (cudaMemsetAsync(dw13, 0, 2ull * E * 2 * F * D, s) != cudaSuccess ||
-            cudaMemsetAsync(dw2, 0, 2ull * E * D * F, s) != cudaSuccess)
+        const bool w2_stage = stage_begin <= MOE_BWD_STAGE_WGRAD_DOWN && MOE_BWD_STAGE_WGRAD_DOWN < stage_end;
+        const bool w13_stage = stage_begin <= MOE_BWD_STAGE_WGRAD_GATE_UP && MOE_BWD_STAGE_WGRAD_GATE_UP < stage_end;
+        if ((w13_stage && cudaMemsetAsync(dw13, 0, 2ull * E * 2 * F * D, s) != cudaSuccess) ||
+            (w2_stage && cudaMemsetAsync(dw2, 0, 2ull * E * D * F, s) != cudaSuccess))
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
@@ -604,7 +607,15 @@ moe_status_t moe_routed_experts_bwd(const void* x, const int32_t* topk_ids, cons
     p.nblk = L.nblk;
     p.padded_rows = L.padded_rows;
     p.sm_count = dev.sm_count;
-    return launch_backward(p, s);
+    return launch_backward(p, stage_begin, stage_end, s);
+}
+
+moe_status_t moe_routed_experts_bwd(const void* x, const int32_t* topk_ids, const void* topk_scores,
+                                    int32_t scores_dtype, const void* w13, const void* w2, const void* dout, void* dx,
+                                    float* dscores, void* dw13, void* dw2, int64_t T, int32_t D, int32_t F, int32_t E,
+                                    int32_t K, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return moe_bwd_stages(x, topk_ids, topk_scores, scores_dtype, w13, w2, dout, dx, dscores, dw13, dw2, T, D, F, E, K,
+                          0, MOE_BWD_STAGES, workspace, workspace_bytes, stream);
 }
 
 moe_status_t moe_fwd_mega_stages(const void* x, const int32_t* topk_ids, const void* topk_scores,

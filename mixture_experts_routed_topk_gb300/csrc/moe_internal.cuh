@@ -148,7 +148,8 @@ struct BwdProblem {
     int64_t padded_rows;
     int sm_count;
 };
-moe_status_t launch_backward(const BwdProblem& p, cudaStream_t stream);
+// Stages [stage_begin, stage_end) of the backward (MOE_BWD_STAGE_*).
+moe_status_t launch_backward(const BwdProblem& p, int stage_begin, int stage_end, cudaStream_t stream);
 
 moe_status_t launch_combine(const void* y, const int32_t* ids, int64_t T, int32_t D, int32_t E, int32_t K,
                             void* out, int sm_count, cudaStream_t stream);

@@ -101,3 +101,33 @@ def test_reference_arm_line(precision):
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == "tiny" and line["config"]["precision"] == precision
+
+
+def test_backward_stage_costs_add_up():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    T, D, F, E, K = 4096, 2048, 1408, 64, 6
+    costs = bench.bwd_stage_costs(T, D, F, E, K, 64)
+    R = T * K
+    assert sum(c["flops"] for c in costs.values()) == 16 * R * D * F  # the whole call's flops
+    assert [s for s in costs if costs[s]["flops"] == 0] == ["dispatch", "reduce"]
+    # the weight-gradient GEMMs write every expert's gradient once
+    assert costs["wgrad_down"]["bytes"] >= E * D * F * 2 and costs["wgrad_gate_up"]["bytes"] >= E * 2 * F * D * 2
+
+
+def test_recorded_traffic_scales_a_cut_capture(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.md").write_text(
+        "| config | kernel | source hash | traffic | read | write | experts touched | note |\n|---|---|---|---|---|---|---|---|\n"
+        "| medium | gemm1_swiglu | 0123456789abcdef | 1000 | 900 | 100 | 64 | x |\n"
+        "| decode (E=16) | gemm1_swiglu | 0123456789abcdef | 1600 | 1500 | 100 | 16 | y |\n"
+        "| decode | gemm2_score | ffffffffffffffff | 5 | 4 | 1 | 16 | stale |\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0123456789abcdef")
+    assert bench.recorded_traffic("medium", "gemm1_swiglu", 64) == 1000.0
+    assert bench.recorded_traffic("decode", "gemm1_swiglu", 222) == 1600 * 222 // 16  # scaled by touched experts
+    assert bench.recorded_traffic("decode", "gemm2_score", 222) is None  # taken on other sources

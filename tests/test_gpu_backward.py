@@ -162,3 +162,32 @@ def test_bwd_no_tokens_gives_zero_weight_gradients():
     binding.moe_routed_experts_bwd(x, ids, sc, w13, w2, x, torch.empty_like(x), sc.clone(), dw13, dw2, ws)
     torch.cuda.synchronize()
     assert torch.count_nonzero(dw13) == 0 and torch.count_nonzero(dw2) == 0
+
+
+@pytest.mark.parametrize("split", [[0, 7], [0, 1, 2, 3, 4, 5, 6, 7], [0, 3, 5, 7]])
+def test_stage_calls_equal_the_whole_call(split):
+    # the backward run as consecutive stage ranges on one workspace gives the whole call's bits
+    d = problem(300, 256, 192, 6, 3)
+    ref, _ = run_bwd(d)
+    x, ids, w13 = d["x"], d["topk_ids"], d["w13"]
+    T, D = x.shape
+    E, _, F, _ = w13.shape
+    K = ids.shape[1]
+    ws = binding.alloc_workspace(binding.moe_bwd_workspace_bytes(T, D, F, E, K), x.device)
+    g = {k: torch.full_like(v, 7) for k, v in ref.items()}
+    for b, e in zip(split[:-1], split[1:]):
+        binding.moe_bwd_stages(x, ids, d["topk_scores"], w13, d["w2"], d["dout"], g["dx"], g["dscores"], g["dw13"],
+                               g["dw2"], ws, b, e)
+    assert binding.moe_get_status(ws) == 0
+    for k in ref:
+        assert torch.equal(g[k], ref[k]), k
+
+
+def test_stage_range_validation():
+    d = problem(16, 128, 128, 4, 2)
+    x, ids, w13 = d["x"], d["topk_ids"], d["w13"]
+    g, ws = run_bwd(d)
+    for b, e in ((-1, 2), (3, 2), (0, 8)):
+        with pytest.raises(binding.MoeError):
+            binding.moe_bwd_stages(x, ids, d["topk_scores"], w13, d["w2"], d["dout"], g["dx"], g["dscores"],
+                                   g["dw13"], g["dw2"], ws, b, e)

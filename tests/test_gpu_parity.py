@@ -45,6 +45,9 @@ CASES = {
     "tail_quarters": (2000, 128, 1024, 23, 1, "uniform"),
     "tail_halves": (2000, 128, 1024, 25, 1, "uniform"),
     "skew": (400, 128, 192, 16, 4, "zipf"),
+    # several 128-token tiles per expert with ragged last tiles of every size class, wide D and F
+    "multi_tile_wide": (600, 320, 384, 4, 2, "uniform"),  # D % 256 = 64; ~300 rows/expert
+    "hot_experts": (2000, 128, 192, 16, 4, "zipf"),  # hot experts with several token tiles
 }
 
 

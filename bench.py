@@ -217,7 +217,8 @@ def kernel_source_hash() -> str:
                 "mixture_experts_routed_topk_gb300/csrc/gemm_pipeline.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/ptx_sm103.cuh",
                 "mixture_experts_routed_topk_gb300/csrc/routing.cu",
-                "mixture_experts_routed_topk_gb300/csrc/combine.cu"):
+                "mixture_experts_routed_topk_gb300/csrc/combine.cu",
+                "mixture_experts_routed_topk_gb300/csrc/backward.cu"):
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

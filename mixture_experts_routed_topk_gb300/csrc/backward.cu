@@ -584,7 +584,8 @@ moe_status_t launch_backward(const BwdProblem& p, int stage_begin, int stage_end
         return st;
     }
 
-    if (run(MOE_BWD_STAGE_REDUCE) && launch_pdl(k_dscores, dim3(grid_for(R, 256, p.sm_count)), dim3(256), 0, stream,
+    if (!run(MOE_BWD_STAGE_REDUCE)) return MOE_OK;
+    if (launch_pdl(k_dscores, dim3(grid_for(R, 256, p.sm_count)), dim3(256), 0, stream,
                    static_cast<const int32_t*>(p.pinv), static_cast<const float*>(p.partial), R,
                    static_cast<int32_t>(ceil_div(F, kBN2)), p.dscores) != cudaSuccess ||
         launch_pdl(k_dx_combine, dim3(grid_for(p.T * (D / 8), 256, p.sm_count)), dim3(256), 0, stream,

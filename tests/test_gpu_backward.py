@@ -183,6 +183,32 @@ def test_stage_calls_equal_the_whole_call(split):
         assert torch.equal(g[k], ref[k]), k
 
 
+def test_each_stage_writes_only_its_outputs():
+    # the stages before the reductions leave dx and dscores untouched; the weight-gradient stages
+    # write dw2 and dw13 and nothing of each other
+    d = problem(300, 256, 192, 6, 3)
+    ref, _ = run_bwd(d)
+    x, ids, w13 = d["x"], d["topk_ids"], d["w13"]
+    T, D = x.shape
+    E, _, F, _ = w13.shape
+    K = ids.shape[1]
+    ws = binding.alloc_workspace(binding.moe_bwd_workspace_bytes(T, D, F, E, K), x.device)
+    g = {k: torch.full_like(v, 7) for k, v in ref.items()}
+    call = lambda b, e: binding.moe_bwd_stages(x, ids, d["topk_scores"], w13, d["w2"], d["dout"], g["dx"],
+                                               g["dscores"], g["dw13"], g["dw2"], ws, b, e)
+    call(0, 4)
+    torch.cuda.synchronize()
+    assert all(torch.all(g[k] == 7) for k in ("dx", "dscores", "dw13", "dw2"))
+    call(4, 5)
+    torch.cuda.synchronize()
+    assert torch.equal(g["dw2"], ref["dw2"]) and torch.all(g["dw13"] == 7) and torch.all(g["dx"] == 7)
+    call(5, 6)
+    torch.cuda.synchronize()
+    assert torch.equal(g["dw13"], ref["dw13"]) and torch.all(g["dx"] == 7) and torch.all(g["dscores"] == 7)
+    call(6, 7)
+    assert torch.equal(g["dx"], ref["dx"]) and torch.equal(g["dscores"], ref["dscores"])
+
+
 def test_stage_range_validation():
     d = problem(16, 128, 128, 4, 2)
     x, ids, w13 = d["x"], d["topk_ids"], d["w13"]

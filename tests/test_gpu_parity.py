@@ -158,6 +158,22 @@ def test_stage_calls_equal_fused_call():
     assert torch.equal(a, out)
 
 
+def test_token_without_valid_pairs_gets_zero_row():
+    d = problem(300, 256, 128, 6, 3)
+    ids = d["topk_ids"].clone()
+    ids[5] = -1  # every pair of token 5 invalid
+    ids[77, :] = 6
+    ids[78, 1] = 9
+    d["topk_ids"] = ids
+    out = torch.full_like(d["x"], float("nan"))
+    ws = binding.alloc_workspace(binding.moe_workspace_bytes(300, 256, 128, 6, 3), "cuda")
+    binding.moe_routed_experts_fwd(d["x"], ids, d["topk_scores"], d["w13"], d["w2"], out, ws)
+    # the combine writes every token's row, a token without any valid pair as zeros
+    assert binding.moe_get_status(ws) & binding.MOE_DEV_BAD_EXPERT_ID
+    assert torch.all(out[5] == 0) and torch.all(out[77] == 0)
+    check_against_oracle(d, out)
+
+
 def test_gather_stage_copies_rows():
     d = problem(90, 192, 128, 5, 3)
     T, D = d["x"].shape

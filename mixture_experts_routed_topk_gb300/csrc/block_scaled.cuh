@@ -4,7 +4,8 @@
 // Both passes place every expert's routed rows from a 128-row boundary ("padded rows"), so a row
 // tile never straddles two experts and its scales are whole 512-byte chunks. A chunk holds the
 // scales of 128 rows for four consecutive blocks along K (row r, block k at byte
-// 16 (r % 32) + 4 (r / 32) + k): the layout tcgen05.cp .32x128b.warpx4 copies into TMEM.
+// 16 (r % 32) + 4 (r / 32) + k): the layout tcgen05.cp .32x128b.warpx4 copies into TMEM (MXFP8),
+// and the one the NVFP4 GEMMs' scale warps store into TMEM lane quarter by lane quarter.
 #pragma once
 
 #include "gemm_pipeline.cuh"

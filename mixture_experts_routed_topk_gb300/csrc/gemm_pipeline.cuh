@@ -14,7 +14,9 @@
 //   Bf16Shape: 4 stages of 16 KB A + 32 KB B (64 bf16 of K), 128 x 256 accumulators, kind::f16.
 //   Nvf4Shape: 5 stages of 16 KB A + 16 KB B (256 packed E2M1 of K) + 4 KB of UE4M3 scale chunks,
 //              128 x 128 accumulators, kind::mxf4nvf4 block-scaled (four scale chunks per operand
-//              per stage, one per K=64 MMA).
+//              per stage, one per K=64 MMA). The scale chunks are loaded on their own barrier and
+//              written into the stage's TMEM slot by four more warps (6-9, one per TMEM lane
+//              quarter) with tcgen05.st, so the MMA thread issues only MMAs.
 //   Mxf8Shape: 4 stages of 16 KB A + 24 KB B (128 E4M3 of K) + their UE8M0 scale chunks (512 B
 //              for A's 128 rows, 1 KB for B's 192 rows), 128 x 192 accumulators (TMEM columns
 //              0..191 and 256..447), kind::mxf8f6f4 block-scaled; the MMA thread copies a stage's
@@ -29,10 +31,14 @@
 //   __device__ static Tile decode(int32_t tile, const GemmArgs&)
 //   __device__ static void load(const Tile&, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
 //                               const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs&)
-//        (block-scaled shapes: load(t, kb, sa, sb, sf, bar, ta, tb, args), sf = the scale chunks)
+//   block-scaled shapes also:
+//   __device__ static void load_scales(const Tile&, int32_t kb, uint8_t* sf, uint64_t* bar,
+//                                      const GemmArgs&)    the stage's A then B scale chunks
 //   __device__ static void epilogue(const Tile&, uint32_t taddr, int row, uint4* stage,
 //                                   const GemmArgs&)          (taddr = this warp's TMEM lanes)
-// Every load() must deliver exactly the shape's kTxBytes (or tx_bytes(t)) into the stage. ta and tb point into the
+// Every load() must deliver exactly the shape's kTxBytes (or tx_bytes(t)) into the stage (with
+// load_scales() when the MMA thread copies the scales; kSfaBytes + kSfbBytes on their own barrier
+// when warps write them). ta and tb point into the
 // kernel's array of four tensor maps (tb == ta + 1); a policy with more operands reads ta[2], ta[3].
 // Optional:
 //   __device__ static bool acquire(const Tile&, const GemmArgs&, volatile int* abort)
@@ -79,6 +85,7 @@ struct Bf16Shape {
     static constexpr int kTxBytes = kABytes + kBBytes;
     static constexpr int kAccCols = moe::kAccCols;
     static constexpr bool kBlockScaled = false;
+    static constexpr bool kScalesByWarps = false;
 };
 
 // E4M3 operands with UE8M0 block scales: kMxBK = 128 K elements (128 bytes, one swizzled row) per
@@ -92,6 +99,8 @@ struct Mxf8Shape {
     static constexpr int kTxBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static constexpr int kAccCols = 256;  // accumulators at TMEM columns 0 and 256, 192 wide each
     static constexpr bool kBlockScaled = true;
+    // the MMA thread copies each stage's scales into the stage's slot (tcgen05.cp)
+    static constexpr bool kScalesByWarps = false;
     // Scale slot of stage s (32 columns: A's scales at +0, B's at +16): in the two gaps after the
     // accumulators, columns 192..255 and 448..511.
     __device__ static constexpr uint32_t sf_slot_col(uint32_t s) { return (s & 2u) * 128u + 192u + 32u * (s & 1u); }
@@ -106,7 +115,13 @@ struct Mxf8Shape {
 
 // Packed E2M1 operands with UE4M3 scales per 16: 256 K elements (128 bytes) per stage, four K=64
 // MMAs, each with its own A and B scale chunk. 128 x 128 accumulators at TMEM columns 0 and 256;
-// 32-column scale slots at 128, 160, 192, 224 and 384 (A's four chunks at +0..+12, B's at +16..+28).
+// 32-column scale slots at 128, 160, 192, 224 and 384, one per stage (A's four chunks at +0..+15,
+// B's at +16..+31).
+//
+// The scales reach TMEM through four scale warps (tcgen05.st), not through tcgen05.cp from the MMA
+// thread: after a tcgen05.cp the MMA thread's next shared-memory access (its wait on the next
+// stage's barrier) stalls until the copies have executed, which left the tensor pipe idle between
+// stages (eight copies per stage here). A stage's scale chunks are loaded on their own barrier.
 constexpr int kNvBN = 128;
 struct Nvf4Shape {
     static constexpr int kStages = 5;
@@ -114,9 +129,10 @@ struct Nvf4Shape {
     static constexpr int kBBytes = kNvBN * 128;         // 16 KB
     static constexpr int kSfaBytes = 2048, kSfbBytes = 2048;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 36 KB
-    static constexpr int kTxBytes = kStageBytes;
+    static constexpr int kTxBytes = kABytes + kBBytes;  // the operand boxes (scales: their own barrier)
     static constexpr int kAccCols = 256;
     static constexpr bool kBlockScaled = true;
+    static constexpr bool kScalesByWarps = true;
     __device__ static constexpr uint32_t sf_slot_col(uint32_t s) { return s < 4u ? 128u + 32u * s : 384u; }
     static constexpr int kSfaChunks = 4, kSfbChunks = 4;
     __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t slot, int kk,
@@ -126,6 +142,9 @@ struct Nvf4Shape {
 };
 static_assert(Nvf4Shape::kStageBytes % 1024 == 0 && Nvf4Shape::kStages == 5, "stage ring / scale slots");
 static_assert(Mxf8Shape::kStageBytes % 1024 == 0 && Mxf8Shape::kTxBytes <= Mxf8Shape::kStageBytes, "stage");
+static_assert(Mxf8Shape::kSfaChunks <= 4 && Mxf8Shape::kSfbChunks <= 4 && Nvf4Shape::kSfaChunks <= 4 &&
+                  Nvf4Shape::kSfbChunks <= 4,
+              "a scale slot holds four chunks of A at columns 0..15 and four of B at 16..31");
 static_assert(Mxf8Shape::kStages == 4 && kMxBN + 64 == Mxf8Shape::kAccCols, "four 32-column scale slots in the gaps");
 
 // The kernel's tensor maps: A and B of the policy's GEMM, then two more for policies that run
@@ -145,6 +164,13 @@ struct ShapeOf<P, std::void_t<typename P::Shape>> {
 };
 constexpr int kGemmThreads = 192;
 constexpr int kEpilogueThreads = 128;
+// Shapes whose scales are written by warps add four warps (one per TMEM lane quarter) that write
+// each K step's scale factors into TMEM.
+constexpr int kScaleWarps = 4;
+template <class S>
+constexpr int gemm_threads() {
+    return kGemmThreads + (S::kScalesByWarps ? 32 * kScaleWarps : 0);
+}
 constexpr int kMnBoxBytes = 64 * kBK * 2;   // one 64 (M or N) x 64 (K) MN-major box: 8 KB
 
 // Epilogue staging: each epilogue warp owns 32 rows x 128 bytes (+16 bytes of padding per row, so
@@ -158,6 +184,8 @@ constexpr int kTileStoreBytes = 48;
 struct alignas(16) PipeState {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
+    uint64_t sf_loaded[kMaxStages];  // scales by warps: the stage's scale chunks are in shared memory
+    uint64_t sf_full[kMaxStages];    // scales by warps: the stage's scales are in its TMEM slot
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -340,7 +368,7 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 }
 
 template <class P>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<typename ShapeOf<P>::type>(), 1)
     k_grouped_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
     using S = typename ShapeOf<P>::type;
     const CUtensorMap* tmap_a = &maps.m[0];
@@ -360,6 +388,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int s = 0; s < S::kStages; ++s) {
             mbar_init(&ps->full[s], 1);
             mbar_init(&ps->empty[s], 1);
+            mbar_init(&ps->sf_loaded[s], 1);
+            mbar_init(&ps->sf_full[s], kScaleWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ps->acc_full[b], 1);
@@ -394,6 +424,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int32_t total = P::num_tiles(args);
     constexpr bool kDynamic = IsDynamic<P>::value;
     static_assert(!HasAcquire<P>::value || kDynamic, "a tile that waits for other tiles needs the dynamic schedule");
+    static_assert(!(kDynamic && S::kScalesByWarps), "the scale warps follow the static schedule");
     static_assert(!kDynamic || (sizeof(typename P::Tile) <= kTileStoreBytes &&
                                 std::is_trivially_copyable<typename P::Tile>::value),
                   "a dynamically scheduled policy's tiles travel through the shared-memory ring");
@@ -447,13 +478,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     uint8_t* sa = smem + s * S::kStageBytes;
+                    if constexpr (S::kScalesByWarps) {  // the small scale chunks first, on their own barrier
+                        mbar_arrive_expect_tx(&ps->sf_loaded[s], S::kSfaBytes + S::kSfbBytes);
+                        P::load_scales(t, kb, sa + S::kABytes + S::kBBytes, &ps->sf_loaded[s], args);
+                    }
                     if constexpr (HasTileShape<P>::value) mbar_arrive_expect_tx(&ps->full[s], P::tx_bytes(t));
                     else mbar_arrive_expect_tx(&ps->full[s], S::kTxBytes);
-                    if constexpr (S::kBlockScaled)
-                        P::load(t, kb, sa, sa + S::kABytes, sa + S::kABytes + S::kBBytes, &ps->full[s], tmap_a,
-                                tmap_b, args);
-                    else
-                        P::load(t, kb, sa, sa + S::kABytes, &ps->full[s], tmap_a, tmap_b, args);
+                    P::load(t, kb, sa, sa + S::kABytes, &ps->full[s], tmap_a, tmap_b, args);
+                    if constexpr (S::kBlockScaled && !S::kScalesByWarps)  // with the operands
+                        P::load_scales(t, kb, sa + S::kABytes + S::kBBytes, &ps->full[s], args);
                     if (!decoded) {
                         if (next < utotal) nt = P::decode(static_cast<int32_t>(next), args);
                         decoded = true;
@@ -518,7 +551,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tcgen05_fence_after_sync();
                     const uint32_t a0 = smem_addr(smem + s * S::kStageBytes);
                     const uint32_t b0 = a0 + S::kABytes;
-                    if constexpr (S::kBlockScaled) {
+                    if constexpr (S::kScalesByWarps) {
+                        // the scale warps have written this stage's scales into its TMEM slot
+                        if (!mbar_wait(&ps->sf_full[s], ph, abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                        tcgen05_fence_after_sync();
+                        const uint32_t slot = tmem_base + S::sf_slot_col(s);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)  // 128-byte stage rows, 32 bytes of K per MMA
+                            S::mma(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
+                                   idesc, slot, kk, (kb | kk) != 0 ? 1u : 0u);
+                    } else if constexpr (S::kBlockScaled) {
                         // this stage's scales into its TMEM slot; the slot's previous reader (the MMAs
                         // of stage use it - kStages) completed before the stage was refilled
                         const uint32_t sf0 = b0 + S::kBBytes;  // A's chunks, then B's, 512 bytes each
@@ -554,6 +599,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 mma_commit(&ps->drain);
                 const unsigned long long t0 = global_timer_ns();
                 while (!mbar_try_wait(&ps->drain, 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+    } else if (warp >= 2 + kEpilogueThreads / 32) {
+        // ------------------------------------------------------------------ scale warps (6-9)
+        // Scales by warps only. For every stage, each warp writes the stage's scale chunks into
+        // the stage's TMEM slot for its own 32-lane quarter: chunk c of A at slot columns
+        // 4c .. 4c+3, chunk c of B at 16 + 4c .. 16 + 4c + 3, lane l of the quarter taking the
+        // chunk's 16 bytes at 16 l (rows l, 32 + l, 64 + l, 96 + l of the chunk's 128 rows, one per
+        // column): the layout the block-scaled MMAs read. The slot's previous reader (the MMAs of
+        // the stage's previous use) completed before the stage was refilled.
+        if constexpr (S::kScalesByWarps) {
+            const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            uint32_t it = 0;
+            bool ok = true;
+            for (uint32_t tcount = 0; ok; ++tcount) {
+                const uint32_t tile = blockIdx.x + tcount * gridDim.x;
+                if (tile >= static_cast<uint32_t>(total)) break;
+                const int32_t kblocks = P::decode(static_cast<int32_t>(tile), args).kblocks;
+                for (int32_t kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % S::kStages;
+                    const uint32_t ph = (it / S::kStages) & 1u;
+                    if (!warp_wait(&ps->sf_loaded[s], ph, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_fence_after_sync();
+                    const uint8_t* sf = smem + s * S::kStageBytes + S::kABytes + S::kBBytes;
+                    uint32_t r[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;
+#pragma unroll
+                    for (int c = 0; c < S::kSfaChunks; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(sf + 512 * c + 16 * lane);
+                        r[4 * c] = v.x, r[4 * c + 1] = v.y, r[4 * c + 2] = v.z, r[4 * c + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int c = 0; c < S::kSfbChunks; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(sf + S::kSfaBytes + 512 * c + 16 * lane);
+                        r[16 + 4 * c] = v.x, r[17 + 4 * c] = v.y, r[18 + 4 * c] = v.z, r[19 + 4 * c] = v.w;
+                    }
+                    tmem_st_32cols(tmem_base + lane_base + S::sf_slot_col(s), r);
+                    tmem_st_wait();
+                    tcgen05_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ps->sf_full[s]);
                 }
             }
         }
@@ -625,7 +716,8 @@ moe_status_t launch_gemm(const GemmMaps& maps, const GemmArgs& a, int grid, cuda
             return MOE_ERR_CUDA;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_grouped_gemm<P>, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, stream, maps, a) ==
+    return launch_pdl(k_grouped_gemm<P>, dim3(grid), dim3(gemm_threads<typename ShapeOf<P>::type>()),
+                      kGemmSmemBytes, stream, maps, a) ==
                    cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;

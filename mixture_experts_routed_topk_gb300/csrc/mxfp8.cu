@@ -231,12 +231,16 @@ struct MxGateUp {
     __device__ static int32_t num_tiles(const GemmArgs& a) { return a.ntn * __ldg(a.tiles + a.E); }
     __device__ static Tile decode(int32_t tile, const GemmArgs& a) { return decode_mx_tile(tile, a); }
 
-    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint8_t* sf, uint64_t* bar,
+    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
                                 const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs& a) {
         const int32_t gate = t.e * 2 * a.F + t.n * kMxGateUpF;
         tma_load_2d(sa, ta, bar, kb * kMxBK, t.row0);
         tma_load_2d(sb, tb, bar, kb * kMxBK, gate);
         tma_load_2d(sb + kMxGateUpF * kMxBK, tb, bar, kb * kMxBK, gate + a.F);
+    }
+    // The stage's scale chunks (A's, then B's), on their own barrier so that they land, and are
+    // written to TMEM, while the operand boxes are still in flight.
+    __device__ static void load_scales(const Tile& t, int32_t kb, uint8_t* sf, uint64_t* bar, const GemmArgs& a) {
         const int64_t groups = a.D / 128;
         bulk_load(sf, a.sf_a + ((t.row0 >> 7) * groups + kb) * 512, 512, bar);
         bulk_load(sf + 512, a.sf_b + ((static_cast<int64_t>(t.e) * a.ntn + t.n) * groups + kb) * 1024, 1024, bar);
@@ -288,10 +292,14 @@ struct MxDown {
     __device__ static int32_t num_tiles(const GemmArgs& a) { return a.ntn * __ldg(a.tiles + a.E); }
     __device__ static Tile decode(int32_t tile, const GemmArgs& a) { return decode_mx_tile(tile, a); }
 
-    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint8_t* sf, uint64_t* bar,
+    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
                                 const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs& a) {
         tma_load_2d(sa, ta, bar, kb * kMxBK, t.row0);
         tma_load_2d(sb, tb, bar, kb * kMxBK, t.e * a.D + t.n * kMxDownN);
+    }
+    // The stage's scale chunks (A's, then B's), on their own barrier so that they land, and are
+    // written to TMEM, while the operand boxes are still in flight.
+    __device__ static void load_scales(const Tile& t, int32_t kb, uint8_t* sf, uint64_t* bar, const GemmArgs& a) {
         const int64_t groups = a.F / 128;
         bulk_load(sf, a.sf_a + ((t.row0 >> 7) * groups + kb) * 512, 512, bar);
         bulk_load(sf + 512, a.sf_b + ((static_cast<int64_t>(t.e) * a.ntn + t.n) * groups + kb) * 1024, 1024, bar);

@@ -12,6 +12,7 @@
 // Kernels, in stream order (weights prepared beforehand: k_nv_amax, k_nv_prepare_weight):
 //   routing -> k_nv_gather_quant (x rows, quantized once per token, at padded rows: packed E2M1 +
 //   UE4M3 chunks)
+//   (both GEMMs: the scale chunks of a stage reach TMEM through four scale warps, tcgen05.st)
 //   -> gate/up GEMM (kind::mxf4nvf4, 128 x 128 tiles of 64 gate + 64 up columns): g and u scaled
 //      by G_x G_w13 in fp32, h = SiLU(g) u quantized per 16 f with G_h -> HQ, HS
 //   -> down GEMM (128 x 128 tiles of D): Y[perm[r]] = score G_h G_w2 acc, bf16
@@ -284,12 +285,16 @@ struct NvGateUp {
     __device__ static int32_t num_tiles(const GemmArgs& a) { return a.ntn * __ldg(a.tiles + a.E); }
     __device__ static Tile decode(int32_t tile, const GemmArgs& a) { return decode_mx_tile(tile, a); }
 
-    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint8_t* sf, uint64_t* bar,
+    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
                                 const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs& a) {
         const int32_t gate = t.e * 2 * a.F + t.n * kNvGateUpF;
         tma_load_2d(sa, ta, bar, kb * 128, t.row0);
         tma_load_2d(sb, tb, bar, kb * 128, gate);
         tma_load_2d(sb + kNvGateUpF * 128, tb, bar, kb * 128, gate + a.F);
+    }
+    // The stage's scale chunks (A's, then B's), on their own barrier so that they land, and are
+    // written to TMEM, while the operand boxes are still in flight.
+    __device__ static void load_scales(const Tile& t, int32_t kb, uint8_t* sf, uint64_t* bar, const GemmArgs& a) {
         const int64_t groups = nv_groups(a.D);
         bulk_load(sf, a.sf_a + ((t.row0 >> 7) * groups + 4 * kb) * 512, 2048, bar);
         bulk_load(sf + 2048, a.sf_b + kNvHeader + ((static_cast<int64_t>(t.e) * a.ntn + t.n) * groups + 4 * kb) * 512,
@@ -340,10 +345,14 @@ struct NvDown {
     __device__ static int32_t num_tiles(const GemmArgs& a) { return a.ntn * __ldg(a.tiles + a.E); }
     __device__ static Tile decode(int32_t tile, const GemmArgs& a) { return decode_mx_tile(tile, a); }
 
-    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint8_t* sf, uint64_t* bar,
+    __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
                                 const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs& a) {
         tma_load_2d(sa, ta, bar, kb * 128, t.row0);
         tma_load_2d(sb, tb, bar, kb * 128, t.e * a.D + t.n * kNvDownN);
+    }
+    // The stage's scale chunks (A's, then B's), on their own barrier so that they land, and are
+    // written to TMEM, while the operand boxes are still in flight.
+    __device__ static void load_scales(const Tile& t, int32_t kb, uint8_t* sf, uint64_t* bar, const GemmArgs& a) {
         const int64_t groups = nv_groups(a.F);
         bulk_load(sf, a.sf_a + ((t.row0 >> 7) * groups + 4 * kb) * 512, 2048, bar);
         bulk_load(sf + 2048, a.sf_b + kNvHeader + ((static_cast<int64_t>(t.e) * a.ntn + t.n) * groups + 4 * kb) * 512,

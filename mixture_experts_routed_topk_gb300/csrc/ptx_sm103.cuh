@@ -1,7 +1,7 @@
 // ptx_sm103.cuh -- inline-PTX wrappers for the Blackwell (sm_103a) asynchronous machinery used
 // by the grouped GEMMs: mbarriers (with bounded waits), TMA tensor loads, tcgen05 tensor-memory
-// allocation, tcgen05.mma (bf16 in, or block-scaled E4M3 / E2M1 in with tcgen05.cp of the scales;
-// fp32 accumulate in TMEM), tcgen05.commit and tcgen05.ld.
+// allocation, tcgen05.mma (bf16 in, or block-scaled E4M3 / E2M1 in with the scales copied or
+// stored into TMEM; fp32 accumulate in TMEM), tcgen05.commit, tcgen05.ld and tcgen05.st.
 //
 // Written from the public PTX ISA (tcgen05 / cp.async.bulk.tensor / mbarrier chapters). Every wait
 // here is bounded: it gives up after kWaitTimeoutNs of wall time, sets MOE_DEV_TIMEOUT in the
@@ -223,7 +223,9 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 // 16 * (r % 32) + 4 * (r / 32) + k. tcgen05.cp .32x128b.warpx4 copies it as 32 rows of 16 bytes
 // into columns c .. c+3 of every 32-lane quarter of TMEM, so the scale of row r sits in column
 // c + r / 32, byte k, of lane r % 32 of each quarter; the MMA's scale-factor id picks byte k. A
-// 256-row operand (B with N > 128) takes two chunks in columns c .. c+7.
+// 256-row operand (B with N > 128) takes two chunks in columns c .. c+7. The same TMEM layout can
+// be written by four warps instead (one per lane quarter, tmem_st_32cols): lane l of each quarter
+// stores the chunk's 16 bytes at 16 l into columns c .. c+3.
 
 // Shared-memory descriptor of one such chunk: no swizzle, 8-row core matrices of 16-byte rows
 // stacked 128 bytes apart (stride-dimension byte offset 128), descriptor version 1.
@@ -305,6 +307,24 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
         : "r"(taddr)
         : "memory");
 }
+
+// Stores 32 consecutive 32-bit columns of this thread's TMEM lane (shape 32x32b, 32 repetitions):
+// thread i of the warp writes lane (taddr.lane + i), columns taddr.col .. taddr.col + 31. The warp
+// may only address its own 32-lane quarter of TMEM (warp index % 4).
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Waits until this thread's outstanding tcgen05.st have written TMEM.
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Waits for this thread's outstanding tcgen05.ld; the register operands tie the loaded values to
 // the wait so the compiler cannot move their uses above it.

@@ -698,6 +698,12 @@ bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows
                uint32_t box_rows);
 
 // The same for a byte tensor (E4M3 codes): inner and box_inner count bytes.
+// A byte tensor [halves, rows, inner] read in boxes of box_inner x box_rows x 2: two consecutive
+// halves (the gate and the up rows of one expert's w13, halves = 2 E) in one copy, written to
+// shared memory as the first half's box_rows rows, then the second's.
+bool make_tmap_u8_pairs(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t halves,
+                        uint32_t box_inner, uint32_t box_rows);
+
 bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                   uint32_t box_rows);
 

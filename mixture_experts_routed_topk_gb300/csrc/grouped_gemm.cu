@@ -391,6 +391,19 @@ bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t r
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_u8_pairs(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t halves,
+                        uint32_t box_inner, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {inner, rows, halves};
+    const cuuint64_t strides[2] = {inner, inner * rows};
+    const cuuint32_t box[3] = {box_inner, box_rows, 2};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count_grid(int64_t max_tiles, int sm_count) {
     const int64_t g = max_tiles < sm_count ? max_tiles : sm_count;
     return static_cast<int>(g > 0 ? g : 1);

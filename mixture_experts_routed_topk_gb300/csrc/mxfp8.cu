@@ -233,10 +233,9 @@ struct MxGateUp {
 
     __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
                                 const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs& a) {
-        const int32_t gate = t.e * 2 * a.F + t.n * kMxGateUpF;
         tma_load_2d(sa, ta, bar, kb * kMxBK, t.row0);
-        tma_load_2d(sb, tb, bar, kb * kMxBK, gate);
-        tma_load_2d(sb + kMxGateUpF * kMxBK, tb, bar, kb * kMxBK, gate + a.F);
+        // the tile's 96 gate rows, then its 96 up rows (halves 2e and 2e + 1), in one copy
+        tma_load_3d(sb, tb, bar, kb * kMxBK, t.n * kMxGateUpF, 2 * t.e);
     }
     // The stage's scale chunks (A's, then B's), on their own barrier so that they land, and are
     // written to TMEM, while the operand boxes are still in flight.
@@ -405,7 +404,7 @@ moe_status_t mx_gate_up(const MxProblem& p, cudaStream_t stream) {
     GemmArgs a = mx_args(p);
     CUtensorMap ta, tb;
     if (!make_tmap_u8(&ta, p.xq, p.D, p.padded_rows, kMxBK, kBM) ||
-        !make_tmap_u8(&tb, p.w13q, p.D, static_cast<uint64_t>(p.E) * 2 * p.F, kMxBK, kMxGateUpF))
+        !make_tmap_u8_pairs(&tb, p.w13q, p.D, p.F, static_cast<uint64_t>(p.E) * 2, kMxBK, kMxGateUpF))
         return MOE_ERR_CUDA;
     a.kblocks = p.D / kMxBK;
     a.ntn = static_cast<int32_t>(ceil_div(p.F, kMxGateUpF));

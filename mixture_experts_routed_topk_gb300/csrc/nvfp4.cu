@@ -287,10 +287,9 @@ struct NvGateUp {
 
     __device__ static void load(const Tile& t, int32_t kb, uint8_t* sa, uint8_t* sb, uint64_t* bar,
                                 const CUtensorMap* ta, const CUtensorMap* tb, const GemmArgs& a) {
-        const int32_t gate = t.e * 2 * a.F + t.n * kNvGateUpF;
         tma_load_2d(sa, ta, bar, kb * 128, t.row0);
-        tma_load_2d(sb, tb, bar, kb * 128, gate);
-        tma_load_2d(sb + kNvGateUpF * 128, tb, bar, kb * 128, gate + a.F);
+        // the tile's 64 gate rows, then its 64 up rows (halves 2e and 2e + 1), in one copy
+        tma_load_3d(sb, tb, bar, kb * 128, t.n * kNvGateUpF, 2 * t.e);
     }
     // The stage's scale chunks (A's, then B's), on their own barrier so that they land, and are
     // written to TMEM, while the operand boxes are still in flight.
@@ -450,7 +449,7 @@ moe_status_t nv_gate_up(const MxProblem& p, cudaStream_t stream) {
     GemmArgs a = nv_args(p);
     CUtensorMap ta, tb;
     if (!make_tmap_u8(&ta, p.xq, p.D / 2, p.padded_rows, 128, kBM) ||
-        !make_tmap_u8(&tb, p.w13q, p.D / 2, static_cast<uint64_t>(p.E) * 2 * p.F, 128, kNvGateUpF))
+        !make_tmap_u8_pairs(&tb, p.w13q, p.D / 2, p.F, static_cast<uint64_t>(p.E) * 2, 128, kNvGateUpF))
         return MOE_ERR_CUDA;
     a.kblocks = nv_groups(p.D) / 4;
     a.ntn = static_cast<int32_t>(ceil_div(p.F, kNvGateUpF));

@@ -277,6 +277,19 @@ struct BwdDgradDown {
         const float s = pair >= 0 ? pair_score(a, pair) : 0.0f;
         const int64_t pitch = 2 * static_cast<int64_t>(a.F) * 2;  // bytes per GU / DGU row
         const char* gu_warp = reinterpret_cast<const char*>(a.in0 + (row - lane) * 2 * a.F);
+        {
+            // this row's g and u lines of every column group into L2 now, so that only the first
+            // group's loads below wait for DRAM (GU does not fit in L2 at these sizes)
+            const char* gu_row = reinterpret_cast<const char*>(a.in0 + row * 2 * a.F);
+#pragma unroll
+            for (int cp = 0; cp < kBN2 / 64; ++cp) {
+                const int32_t f0 = t.n * kBN2 + cp * 64;
+                if (f0 < a.F) {
+                    prefetch_l2(gu_row + 2 * f0);
+                    prefetch_l2(gu_row + 2 * (a.F + f0));
+                }
+            }
+        }
         float partial = 0.0f;
 #pragma unroll 1
         for (int cp = 0; cp < kBN2 / 64; ++cp) {

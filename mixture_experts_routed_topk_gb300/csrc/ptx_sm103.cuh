@@ -137,6 +137,11 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// Asks L2 to fetch the 128-byte line holding `p` (no register result, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both addresses 16-byte aligned),
 // completion signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {

@@ -189,6 +189,20 @@ def test_nvfp4_forward_matches_oracle(name):
     assert err <= OUT_TOL, (name, err)
 
 
+def test_nvfp4_every_pair_on_two_experts():
+    # experts 0 and E-1 take every pair (six row tiles each, many column tiles and K steps in a
+    # row through the same stages and scale slots); the other experts are empty
+    T, D, F, E, K = 700, 512, 384, 8, 2
+    ids = torch.zeros((T, K), dtype=torch.int32)
+    ids[:, 1] = E - 1
+    d = problem(T, D, F, E, K, seed=5, ids=ids)
+    out, ws = run_nv(d)
+    assert binding.moe_get_status(ws) == 0
+    ref, _ = oracle_nv_tokens(d)
+    err = max_rel_err(out.float().cpu().numpy(), ref)
+    assert err <= OUT_TOL, err
+
+
 @pytest.mark.parametrize("T", [300, 2100])  # 1024-column work items, and whole rows (T >= 2048)
 def test_activation_rows_bit_exact_and_padding_scales_zero(T):
     D, F, E, K = 640, 256, 6, 3  # D leaves two padding scale groups per row
